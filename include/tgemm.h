@@ -1,0 +1,196 @@
+/*
+ * tgemm.h -- C ABI of the software-pipelined tiled GEMM for GB300 (sm_103a).
+ *
+ * The operation.  C[M,N] = A[M,K] . B[N,K]^T with fp16 or bf16 operands,
+ * fp32 accumulation, and C either fp32 (the raw accumulator) or the operand
+ * dtype (fp32 rounded to nearest even).  This is the tiled GEMM of the
+ * TileLang tutorial, chapter 11 "Pipeline and autotuning": section 1.1 gives
+ * the tiled body (per output tile, clear an fp32 accumulator, loop over K in
+ * block_K steps copying an A tile and a B tile into shared memory and
+ * multiplying with transpose_B), section 3.5 gives the kernel signature
+ * (A:(M,K), B:(N,K), C:(M,N); tile block_M x block_N x block_K; num_stages),
+ * and section 2.3 / 4.4 give the pipelining: num_stages copies of each
+ * operand tile, slot ko % num_stages, so that loads of k-block ko+1.. overlap
+ * the math of k-block ko.
+ *
+ * Memory.  Every matrix is dense and row-major: A is M x K (K contiguous),
+ * B is N x K (K contiguous), C is M x N (N contiguous).  Device pointers are
+ * owned by the caller and must be 16-byte aligned; the library never
+ * allocates or frees them.  The row pitch of every matrix must be a multiple
+ * of 16 bytes (K % 8 == 0; N % 4 == 0 for fp32 C, N % 8 == 0 for 16-bit C),
+ * as the tensor-memory-access engine requires.
+ *
+ * Errors.  Every function returns a tgemm_status_code (0 = TGEMM_OK) or a
+ * value documented below; nothing throws across this boundary and nothing
+ * aborts the process.  Arguments are checked before anything is launched.
+ *
+ * Threads.  A plan may be used from one host thread at a time.  Different
+ * plans are independent.
+ */
+#ifndef TGEMM_H
+#define TGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same object as cudaStream_t / CUstream); NULL is
+ * the legacy default stream. */
+typedef struct CUstream_st *tgemm_stream_t;
+
+/* Opaque plan: validated shape, tile, depth and launch configuration. */
+typedef struct tgemm_plan_s *tgemm_plan_t;
+
+enum tgemm_dtype {
+    TGEMM_F16 = 0,  /* IEEE binary16 */
+    TGEMM_BF16 = 1, /* bfloat16 */
+    TGEMM_F32 = 2   /* IEEE binary32, output only */
+};
+
+enum tgemm_status_code {
+    TGEMM_OK = 0,
+    TGEMM_ERR_INVALID_ARG = 1,       /* a size, pointer or config outside its documented range */
+    TGEMM_ERR_UNSUPPORTED_DTYPE = 2, /* dtype not F16/BF16, or out_dtype not F32/dtype */
+    TGEMM_ERR_ALIGNMENT = 3,         /* pointer or row pitch not a multiple of 16 bytes */
+    TGEMM_ERR_SMEM_BUDGET = 4,       /* tile x num_stages does not fit in shared memory */
+    TGEMM_ERR_NO_KERNEL = 5,         /* tile shape the kernel does not implement */
+    TGEMM_ERR_ARCH = 6,              /* current device is not compute capability 10.3 */
+    TGEMM_ERR_CUDA = 7,              /* a CUDA runtime or driver call failed */
+    TGEMM_ERR_TIMEOUT = 8            /* a pipeline wait inside the kernel ran out of time */
+};
+
+/*
+ * Shared-memory upper bound of the pipeline, in bytes: num_stages copies of
+ * one A tile (block_M x block_K) and one B tile (block_K x block_N), times the
+ * element size of dtype.  Chapter 11, section 4.5 ("multi-buffering and the
+ * on-chip capacity limit").  Returns -TGEMM_ERR_UNSUPPORTED_DTYPE or
+ * -TGEMM_ERR_INVALID_ARG (negative) on bad input.  Host only; needs no GPU.
+ */
+int64_t tgemm_smem_bound(int dtype, int block_M, int block_N, int block_K, int num_stages);
+
+/*
+ * Dynamic shared memory the kernel actually requests for this config, in
+ * bytes: the pipeline ring (the bound above, each slot aligned for the
+ * swizzled layout), the output staging buffers, the ring's full/empty
+ * barriers, the accumulator barriers and alignment slack.  Negative status
+ * on bad input, as above.  Host only.
+ */
+int64_t tgemm_smem_bytes(int dtype, int out_dtype, int block_M, int block_N, int block_K,
+                         int num_stages);
+
+/*
+ * Per-block shared-memory limit (cudaDevAttrMaxSharedMemoryPerBlockOptin) of
+ * the current device, in bytes; negative status if no device can be queried.
+ */
+int tgemm_smem_limit(void);
+
+/*
+ * Validate a problem and config against a given per-block shared-memory
+ * limit, without touching a GPU: the same checks tgemm_plan makes, in the
+ * same order, with `smem_limit` standing in for the queried device limit.
+ *   - dtype in {F16, BF16}, out_dtype in {F32, dtype}     -> UNSUPPORTED_DTYPE
+ *   - M, N >= 0, K >= 0, each < 2^31; num_stages >= 1      -> INVALID_ARG
+ *   - K % 8 == 0, N * out_bytes % 16 == 0 (row pitch)      -> ALIGNMENT
+ *   - block_M in {128, 256}; block_N a multiple of 32 in
+ *     [32, 256]; block_K in {16, 32, 64} (16-bit operands:
+ *     rows of 32, 64 or 128 bytes)                          -> NO_KERNEL
+ *   - tgemm_smem_bound > smem_limit or
+ *     tgemm_smem_bytes > smem_limit                         -> SMEM_BUDGET
+ * The budget rule is the one of chapter 11 sections 4.5 and 5.1: a config
+ * over budget is rejected before anything is launched, rather than failing
+ * at launch.  M == 0 or N == 0 is a valid empty product; K == 0 is a valid
+ * empty reduction (C is all zeros).
+ */
+int tgemm_validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M,
+                   int block_N, int block_K, int num_stages, int64_t smem_limit);
+
+/*
+ * Create a plan on the current CUDA device.  Runs tgemm_validate with the
+ * device's queried limit, checks that the device is sm_103 (ERR_ARCH),
+ * allocates a 16-byte device status word owned by the plan, and sets the
+ * kernel's dynamic shared-memory attribute.  On success *out is a plan owned
+ * by the caller (free it with tgemm_destroy); on failure *out is NULL.  The
+ * pages' analogue is matmul(M, N, K, block_M, block_N, block_K, num_stages,
+ * ...) of chapter 11 section 3.5; its `threads` argument has no counterpart
+ * because the kernel's warp roles fix the block at 192 threads.
+ */
+int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
+               int block_M, int block_N, int block_K, int num_stages);
+
+/*
+ * Enqueue C = A . B^T on `stream`.  A, B, C are device pointers with the
+ * layouts above (16-byte aligned, caller-owned; C must not overlap A or B).
+ * Returns after the launch is enqueued; results are ready when the stream
+ * has run it.  The pages' analogue is kernel(A, B, C) with C the output.
+ * ERR_INVALID_ARG for a NULL plan or pointer (unless the product is empty),
+ * ERR_ALIGNMENT for a misaligned pointer, ERR_CUDA if the launch fails.
+ */
+int tgemm_run(tgemm_plan_t plan, const void *A, const void *B, void *C, tgemm_stream_t stream);
+
+/*
+ * End-to-end form of tgemm_run for operands in host memory: enqueue on
+ * `stream` the copies hA -> dA and hB -> dB, the GEMM into dC, and the copy
+ * dC -> hC.  hA/hB/hC are host buffers of the same layouts (page-locked
+ * memory makes the copies asynchronous); dA/dB/dC are caller-owned device
+ * buffers of the same sizes.  The library allocates nothing.  Returns after
+ * enqueueing; hC is valid once the stream has run.  Errors as tgemm_run.
+ */
+int tgemm_run_host(tgemm_plan_t plan, const void *hA, const void *hB, void *hC, void *dA,
+                   void *dB, void *dC, tgemm_stream_t stream);
+
+/*
+ * Read and clear the plan's device status word.  Call after the stream that
+ * ran the plan has been synchronised (this call itself synchronises through
+ * a blocking copy).  Returns TGEMM_OK, or TGEMM_ERR_TIMEOUT if a pipeline
+ * wait in any CTA ran past the watchdog limit (the kernel then stops its
+ * pipeline, waits for its copies in flight, frees its tensor memory and
+ * returns instead of hanging; C is undefined).  Negative ERR_CUDA on a failed
+ * copy.  `detail` (may be NULL) receives 4 ints: code, warp role (0 producer,
+ * 1 MMA, 2 epilogue), block index, and the pipeline iteration that timed out.
+ */
+int tgemm_status(tgemm_plan_t plan, int *detail);
+
+/*
+ * Watchdog limit of every in-kernel pipeline wait, in nanoseconds of
+ * %globaltimer (default 2e9, or the environment variable TGEMM_WATCHDOG_NS
+ * read at plan time).  0 restores the default.
+ */
+int tgemm_set_watchdog_ns(tgemm_plan_t plan, uint64_t ns);
+
+/*
+ * Test hook: when `on` is nonzero, the MMA warp of every CTA waits, at its
+ * first k-block, on a barrier that nothing arrives on, so that the watchdog
+ * path runs (status TGEMM_ERR_TIMEOUT).  No fault, trap or hang results.
+ */
+int tgemm_debug_stall(tgemm_plan_t plan, int on);
+
+/* Launch geometry and resources of a plan (for reports and the sweep). */
+typedef struct tgemm_plan_info {
+    int64_t M, N, K;
+    int dtype, out_dtype, block_M, block_N, block_K, num_stages;
+    int tiles_m, tiles_n, num_tiles, grid, threads;
+    int num_k_blocks;    /* ceil(K / block_K) */
+    int acc_stages;      /* accumulator buffers in tensor memory (1 or 2) */
+    int tmem_columns;    /* tensor-memory columns allocated per CTA */
+    int64_t smem_bytes;  /* dynamic shared memory requested per CTA */
+    int64_t smem_bound;  /* the pages' num_stages * (A + B tile) bound */
+    int smem_limit;      /* device per-block limit at plan time */
+    int num_sms;
+} tgemm_plan_info;
+
+int tgemm_get_plan_info(tgemm_plan_t plan, tgemm_plan_info *info);
+
+/* Free a plan and its status word.  NULL is accepted (no-op). */
+int tgemm_destroy(tgemm_plan_t plan);
+
+/* Static text for a status code (never NULL). */
+const char *tgemm_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TGEMM_H */

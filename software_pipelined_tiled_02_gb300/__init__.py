@@ -1,0 +1,297 @@
+"""Software-pipelined tiled GEMM for GB300: Python binding of ``libtgemm.so``.
+
+``C[M,N] = A[M,K] . B[N,K]^T`` with fp16/bf16 operands and fp32 accumulation,
+computed by the hand-written sm_103a kernel behind the C ABI declared in
+``include/tgemm.h``.  This module only marshals arguments: it passes torch
+tensors' device pointers and CUDA streams to the library and maps status
+codes to exceptions.  There is no fallback: if ``libtgemm.so`` is missing or
+fails to load, every call raises.
+
+The same names as the C ABI are exported (``tgemm_plan`` ... ``tgemm_strerror``)
+plus a ``Plan`` wrapper and ``gemm()``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtgemm.so")
+
+F16, BF16, F32 = 0, 1, 2
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DTYPE, ERR_ALIGNMENT, ERR_SMEM_BUDGET, ERR_NO_KERNEL, ERR_ARCH, ERR_CUDA, \
+    ERR_TIMEOUT = range(9)
+_DT_NAMES = {"f16": F16, "bf16": BF16, "f32": F32}
+
+SYMBOLS = ("tgemm_smem_bound", "tgemm_smem_bytes", "tgemm_smem_limit", "tgemm_validate", "tgemm_plan",
+           "tgemm_run", "tgemm_run_host", "tgemm_status", "tgemm_set_watchdog_ns", "tgemm_debug_stall",
+           "tgemm_get_plan_info", "tgemm_destroy", "tgemm_strerror")
+
+
+class TgemmError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} (code {code})" if what else strerror(code))
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("block_M", ctypes.c_int),
+                ("block_N", ctypes.c_int), ("block_K", ctypes.c_int), ("num_stages", ctypes.c_int),
+                ("tiles_m", ctypes.c_int), ("tiles_n", ctypes.c_int), ("num_tiles", ctypes.c_int),
+                ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("num_k_blocks", ctypes.c_int),
+                ("acc_stages", ctypes.c_int), ("tmem_columns", ctypes.c_int), ("smem_bytes", ctypes.c_int64),
+                ("smem_bound", ctypes.c_int64), ("smem_limit", ctypes.c_int), ("num_sms", ctypes.c_int)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load ``libtgemm.so`` (raises if it is absent: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libtgemm.so not built at {path}; run software_pipelined_tiled_02_gb300/build.py "
+                               "or __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        L.tgemm_smem_bound.argtypes = [i32] * 5
+        L.tgemm_smem_bound.restype = i64
+        L.tgemm_smem_bytes.argtypes = [i32] * 6
+        L.tgemm_smem_bytes.restype = i64
+        L.tgemm_smem_limit.argtypes = []
+        L.tgemm_smem_limit.restype = i32
+        L.tgemm_validate.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, i64]
+        L.tgemm_validate.restype = i32
+        L.tgemm_plan.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i32, i32, i32, i32, i32, i32]
+        L.tgemm_plan.restype = i32
+        L.tgemm_run.argtypes = [vp, vp, vp, vp, vp]
+        L.tgemm_run.restype = i32
+        L.tgemm_run_host.argtypes = [vp] * 8
+        L.tgemm_run_host.restype = i32
+        L.tgemm_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+        L.tgemm_status.restype = i32
+        L.tgemm_set_watchdog_ns.argtypes = [vp, ctypes.c_uint64]
+        L.tgemm_set_watchdog_ns.restype = i32
+        L.tgemm_debug_stall.argtypes = [vp, i32]
+        L.tgemm_debug_stall.restype = i32
+        L.tgemm_get_plan_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+        L.tgemm_get_plan_info.restype = i32
+        L.tgemm_destroy.argtypes = [vp]
+        L.tgemm_destroy.restype = i32
+        L.tgemm_strerror.argtypes = [i32]
+        L.tgemm_strerror.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def _dt(x) -> int:
+    if isinstance(x, int):
+        return x
+    if isinstance(x, str):
+        return _DT_NAMES[x]
+    import torch
+
+    return {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32}[x]
+
+
+def _torch_dtype(code: int):
+    import torch
+
+    return {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}[code]
+
+
+# ------------------------------------------------------------- C ABI names
+
+def tgemm_smem_bound(dtype, block_M, block_N, block_K, num_stages) -> int:
+    return int(load().tgemm_smem_bound(_dt(dtype), block_M, block_N, block_K, num_stages))
+
+
+def tgemm_smem_bytes(dtype, out_dtype, block_M, block_N, block_K, num_stages) -> int:
+    return int(load().tgemm_smem_bytes(_dt(dtype), _dt(out_dtype), block_M, block_N, block_K, num_stages))
+
+
+def tgemm_smem_limit() -> int:
+    return int(load().tgemm_smem_limit())
+
+
+def tgemm_validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit) -> int:
+    return int(load().tgemm_validate(M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K, num_stages,
+                                     smem_limit))
+
+
+def tgemm_plan(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages):
+    """Returns ``(status, handle)``; handle is None on failure."""
+    h = ctypes.c_void_p()
+    rc = load().tgemm_plan(ctypes.byref(h), M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K,
+                           num_stages)
+    return int(rc), (h if rc == OK else None)
+
+
+def tgemm_run(plan, A_ptr: int, B_ptr: int, C_ptr: int, stream: int = 0) -> int:
+    return int(load().tgemm_run(plan, A_ptr, B_ptr, C_ptr, stream))
+
+
+def tgemm_run_host(plan, hA: int, hB: int, hC: int, dA: int, dB: int, dC: int, stream: int = 0) -> int:
+    return int(load().tgemm_run_host(plan, hA, hB, hC, dA, dB, dC, stream))
+
+
+def tgemm_status(plan):
+    d = (ctypes.c_int * 4)()
+    rc = load().tgemm_status(plan, d)
+    return int(rc), list(d)
+
+
+def tgemm_set_watchdog_ns(plan, ns: int) -> int:
+    return int(load().tgemm_set_watchdog_ns(plan, ns))
+
+
+def tgemm_debug_stall(plan, on: bool) -> int:
+    return int(load().tgemm_debug_stall(plan, 1 if on else 0))
+
+
+def tgemm_get_plan_info(plan) -> dict:
+    info = PlanInfo()
+    rc = load().tgemm_get_plan_info(plan, ctypes.byref(info))
+    if rc != OK:
+        raise TgemmError(rc, "tgemm_get_plan_info")
+    return info.as_dict()
+
+
+def tgemm_destroy(plan) -> int:
+    return int(load().tgemm_destroy(plan))
+
+
+def strerror(code: int) -> str:
+    try:
+        return load().tgemm_strerror(int(code)).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+tgemm_strerror = strerror
+
+
+# ------------------------------------------------------------- conveniences
+
+class Plan:
+    """A validated GEMM configuration on the current CUDA device."""
+
+    def __init__(self, M, N, K, dtype="f16", out_dtype=None, block=(128, 256, 64), num_stages=4):
+        dtype = _dt(dtype)
+        out_dtype = dtype if out_dtype is None else _dt(out_dtype)
+        bm, bn, bk = block
+        rc, h = tgemm_plan(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages)
+        if rc != OK:
+            raise TgemmError(rc, f"tgemm_plan(M={M}, N={N}, K={K}, block={block}, num_stages={num_stages})")
+        self.handle = h
+        self.M, self.N, self.K = M, N, K
+        self.dtype, self.out_dtype = dtype, out_dtype
+        self.block, self.num_stages = tuple(block), num_stages
+
+    @property
+    def info(self) -> dict:
+        return tgemm_get_plan_info(self.handle)
+
+    def _check(self, A, B, C):
+        import torch
+
+        for name, t, shape, dt in (("A", A, (self.M, self.K), self.dtype), ("B", B, (self.N, self.K), self.dtype),
+                                   ("C", C, (self.M, self.N), self.out_dtype)):
+            if t.dtype != _torch_dtype(dt):
+                raise TypeError(f"{name} must be {_torch_dtype(dt)}, got {t.dtype}")
+            if tuple(t.shape) != shape:
+                raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous (row-major)")
+        if not (A.is_cuda and B.is_cuda and C.is_cuda):
+            raise ValueError("A, B and C must be CUDA tensors")
+        if not (A.device == B.device == C.device == torch.device("cuda", torch.cuda.current_device())):
+            raise ValueError("A, B, C must be on the current CUDA device")
+
+    def run(self, A, B, C=None, stream=None):
+        """Enqueue ``C = A . B^T`` on ``stream`` (default: torch's current stream); returns C."""
+        import torch
+
+        if C is None:
+            C = torch.empty((self.M, self.N), dtype=_torch_dtype(self.out_dtype), device=A.device)
+        self._check(A, B, C)
+        s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        rc = tgemm_run(self.handle, A.data_ptr(), B.data_ptr(), C.data_ptr(), s)
+        if rc != OK:
+            raise TgemmError(rc, "tgemm_run")
+        return C
+
+    def run_host(self, hA, hB, hC, dA, dB, dC, stream=None):
+        """Host operands in, host result out (copies enqueued by the library)."""
+        import torch
+
+        s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        rc = tgemm_run_host(self.handle, hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), dA.data_ptr(),
+                            dB.data_ptr(), dC.data_ptr(), s)
+        if rc != OK:
+            raise TgemmError(rc, "tgemm_run_host")
+        return hC
+
+    def status(self):
+        """Read and clear the device status word; (code, detail)."""
+        return tgemm_status(self.handle)
+
+    def set_watchdog_ns(self, ns: int):
+        tgemm_set_watchdog_ns(self.handle, ns)
+
+    def debug_stall(self, on: bool):
+        tgemm_debug_stall(self.handle, on)
+
+    def close(self):
+        if self.handle is not None:
+            tgemm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+_plans: dict = {}
+
+
+def default_config(M, N, K, dtype="f16", out_dtype=None):
+    """The tuned default (block, num_stages) for a shape."""
+    from . import defaults
+
+    return defaults.choose(M, N, K, _dt(dtype), _dt(dtype) if out_dtype is None else _dt(out_dtype))
+
+
+def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=None):
+    """``A[M,K] . B[N,K]^T`` on the GPU through ``libtgemm.so``.
+
+    ``out_dtype`` defaults to the operand dtype; ``torch.float32`` returns the
+    raw fp32 accumulator.  ``block``/``num_stages`` default to the tuned table.
+    """
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("A and B must agree on K")
+    dt = _dt(A.dtype)
+    odt = dt if out_dtype is None else _dt(out_dtype)
+    if block is None or num_stages is None:
+        b, s = default_config(M, N, K, dt, odt)
+        block = block or b
+        num_stages = num_stages or s
+    key = (M, N, K, dt, odt, tuple(block), num_stages, A.device.index)
+    plan = _plans.get(key)
+    if plan is None:
+        plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages)
+    return plan.run(A, B, out, stream)

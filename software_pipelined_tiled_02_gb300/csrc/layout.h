@@ -1,0 +1,116 @@
+// layout.h -- tile configurations, the shared-memory plan of one CTA, and
+// argument validation for the pipelined GEMM.  Pure host/device C++ with no
+// CUDA calls, so the same rules are usable without a GPU.
+#pragma once
+
+#include <cstdint>
+
+namespace tg {
+
+// Status codes (mirror of tgemm_status_code in the public header).
+enum : int {
+    kOk = 0,
+    kErrInvalidArg = 1,
+    kErrUnsupportedDtype = 2,
+    kErrAlignment = 3,
+    kErrSmemBudget = 4,
+    kErrNoKernel = 5,
+    kErrArch = 6,
+    kErrCuda = 7,
+    kErrTimeout = 8,
+};
+
+enum : int { kF16 = 0, kBF16 = 1, kF32 = 2 };
+
+constexpr int kThreads = 192;         // 6 warps: TMA producer, MMA issuer, 4 epilogue warps
+constexpr int kEpiWarps = 4;
+constexpr int kEpiCols = 32;          // accumulator columns per epilogue chunk
+constexpr int kEpiBufs = 2;           // staging buffers per epilogue warp
+constexpr int kTmemColsMax = 512;     // tensor-memory columns per SM
+constexpr uint32_t kSmemAlign = 1024; // swizzle-atom alignment of every tile slot
+
+inline int dtype_bytes(int dt) { return dt == kF32 ? 4 : (dt == kF16 || dt == kBF16) ? 2 : 0; }
+
+struct Layout {
+    int bm, bn, bk, stages;
+    int in_bytes, out_bytes;
+    uint32_t a_stage_bytes;  // bm * bk * in_bytes
+    uint32_t b_stage_bytes;  // bn * bk * in_bytes
+    uint32_t c_buf_bytes;    // one staging buffer: 32 rows x kEpiCols x out_bytes
+    uint32_t off_a, off_b, off_c, off_bar;
+    uint32_t bar_bytes;
+    uint32_t total;          // bytes requested, including alignment slack
+    int64_t bound;           // stages * (A tile + B tile): the budget rule's bound
+    int m_halves;            // bm / 128 MMAs of M = 128 per k-step
+    int acc_cols;            // TMEM columns of one accumulator (m_halves * bn)
+    int acc_stages;          // accumulators in flight (2 lets the epilogue overlap the next tile)
+    int tmem_cols;           // power of two >= 32 allocated per CTA
+    int swizzle_bytes;       // operand row bytes = bk * in_bytes: 32, 64 or 128
+};
+
+inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Tile shapes the kernel implements: M = 128 MMAs (one or two per k-step),
+// N a multiple of 32 up to the MMA maximum of 256, and block_K such that a
+// K-contiguous operand row is exactly one swizzle span (32, 64 or 128 bytes).
+inline bool tile_supported(int bm, int bn, int bk, int in_bytes)
+{
+    if (bm != 128 && bm != 256) return false;
+    if (bn < 32 || bn > 256 || bn % 32 != 0) return false;
+    int row = bk * in_bytes;
+    return (row == 32 || row == 64 || row == 128) && bk > 0;
+}
+
+// Barrier block: full[S], empty[S], acc_full[2], acc_empty[2], drain, stall
+// (8 bytes each), then the TMEM base address word and the abort flag.
+inline uint32_t barrier_block_bytes(int stages) { return round_up((2u * stages + 6u) * 8u + 8u, 16u); }
+
+inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out_dtype)
+{
+    Layout L{};
+    L.bm = bm;
+    L.bn = bn;
+    L.bk = bk;
+    L.stages = stages;
+    L.in_bytes = dtype_bytes(dtype);
+    L.out_bytes = dtype_bytes(out_dtype);
+    L.a_stage_bytes = uint32_t(bm) * bk * L.in_bytes;
+    L.b_stage_bytes = uint32_t(bn) * bk * L.in_bytes;
+    L.bound = int64_t(stages) * (int64_t(bm) * bk + int64_t(bk) * bn) * L.in_bytes;
+    L.c_buf_bytes = 32u * kEpiCols * L.out_bytes;
+    L.off_a = 0;
+    L.off_b = L.off_a + uint32_t(stages) * round_up(L.a_stage_bytes, kSmemAlign);
+    L.off_c = L.off_b + uint32_t(stages) * round_up(L.b_stage_bytes, kSmemAlign);
+    L.off_bar = L.off_c + round_up(uint32_t(kEpiWarps * kEpiBufs) * L.c_buf_bytes, kSmemAlign);
+    L.bar_bytes = barrier_block_bytes(stages);
+    L.total = L.off_bar + L.bar_bytes + kSmemAlign;  // slack to align the dynamic base
+    L.m_halves = bm / 128;
+    L.acc_cols = L.m_halves * bn;
+    L.acc_stages = (2 * L.acc_cols <= kTmemColsMax) ? 2 : 1;
+    int need = L.acc_stages * L.acc_cols;
+    int cols = 32;
+    while (cols < need) cols <<= 1;
+    L.tmem_cols = cols;
+    L.swizzle_bytes = bk * L.in_bytes;
+    return L;
+}
+
+// Every check of tgemm_validate, in the documented order.
+inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int bm, int bn, int bk,
+                    int stages, int64_t smem_limit)
+{
+    if (dtype != kF16 && dtype != kBF16) return kErrUnsupportedDtype;
+    if (out_dtype != kF32 && out_dtype != dtype) return kErrUnsupportedDtype;
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim) return kErrInvalidArg;
+    if (stages < 1) return kErrInvalidArg;
+    if ((K * dtype_bytes(dtype)) % 16 != 0) return kErrAlignment;
+    if ((N * dtype_bytes(out_dtype)) % 16 != 0) return kErrAlignment;
+    if (!tile_supported(bm, bn, bk, dtype_bytes(dtype))) return kErrNoKernel;
+    if (stages > 64) return kErrSmemBudget;  // keeps the layout arithmetic in 32 bits
+    Layout L = make_layout(bm, bn, bk, stages, dtype, out_dtype);
+    if (L.bound > smem_limit || int64_t(L.total) > smem_limit) return kErrSmemBudget;
+    return kOk;
+}
+
+}  // namespace tg

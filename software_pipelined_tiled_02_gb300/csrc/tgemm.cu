@@ -1,0 +1,755 @@
+// tgemm.cu -- software-pipelined tiled GEMM for GB300 (sm_103a) and its C ABI.
+//
+// C[M,N] = A[M,K] . B[N,K]^T, fp16/bf16 operands, fp32 accumulation in tensor
+// memory, fp32 or 16-bit output.  The computation is the tiled GEMM of the
+// TileLang tutorial, chapter 11 "Pipeline and autotuning" (section 1.1: per
+// output tile, clear an fp32 accumulator, walk K in block_K steps, copy an A
+// tile and a B tile to shared memory, multiply with transpose_B, write the
+// tile out).  Its pipelining (sections 2.3, 4.3, 4.4, 5.2) is realised here
+// for Blackwell rather than by a compiler pass:
+//
+//  * the num_stages multi-buffer ("version dimension", slot ko % num_stages)
+//    is a ring of num_stages shared-memory slots, each holding one A tile and
+//    one B tile in the 32/64/128-byte swizzled K-major layout that both the
+//    TMA engine writes and the tensor core reads;
+//  * the synchronisation rule of section 5.2 (before writing slot s wait for
+//    its last reader; before reading slot s wait for its writer) is a pair of
+//    mbarriers per slot: full[s] completes when the TMA bytes of the slot have
+//    landed (transaction count), empty[s] completes when the MMAs that read
+//    the slot have finished (tcgen05.commit);
+//  * the prologue / steady state / epilogue of section 4.3 are implicit: the
+//    producer warp runs up to num_stages k-blocks ahead of the MMA warp and
+//    blocks only on empty[s];
+//  * num_stages = 1 is the unpipelined control of section 1.1 (copy and math
+//    serialise on the single slot).
+//
+// Warp roles (192 threads, one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer (one thread)
+//   warp 1      TMEM allocator and tcgen05.mma issuer (one thread)
+//   warps 2..5  epilogue: TMEM -> registers -> swizzled shared staging -> TMA store
+// The accumulator is double-buffered in TMEM when it fits, so the epilogue of
+// tile i overlaps the main loop of tile i+1.  The summation order inside a
+// tile depends only on the tile shape (k-block by k-block, 16 at a time), never
+// on num_stages or the schedule, so results are bit-identical across depths.
+//
+// Every mbarrier wait is bounded by a %globaltimer watchdog: on expiry the
+// kernel records TGEMM_ERR_TIMEOUT in the plan's status word, stops issuing
+// work, waits (bounded) for its copies and MMAs in flight, frees its tensor
+// memory and returns.  Nothing traps.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "layout.h"
+#include "ptx.cuh"
+#include "tgemm.h"
+
+namespace tg {
+
+struct Params {  // 64-byte aligned through its CUtensorMap members
+    CUtensorMap tmA, tmB, tmC;
+    int M, N, K;
+    int num_kb;                 // ceil(K / bk)
+    int tiles_m, tiles_n, num_tiles, group_m;
+    int bm, bn, bk, stages;
+    int n_kstep;                // bk / 16 MMAs along K per slot
+    int m_halves;               // bm / 128
+    int out_mode;               // 0 fp32, 1 fp16, 2 bf16
+    int acc_stages, acc_cols, tmem_cols;
+    uint32_t idesc;             // tcgen05 instruction descriptor (kind::f16)
+    uint32_t a_slot, b_slot;    // bytes between consecutive ring slots
+    uint32_t stage_tx;          // bytes the TMA delivers per slot (A box + B box)
+    uint32_t row_bytes;         // bytes of one K-contiguous operand row in a slot
+    uint32_t off_a, off_b, off_c, off_bar, c_buf_bytes;
+    uint32_t desc_lo_flags;     // leading-byte-offset field of the smem descriptor
+    uint32_t desc_hi;           // high word: stride byte offset, version, swizzle mode
+    unsigned long long watchdog_ns;
+    int *status;                // 4 ints: code, role, block, iteration
+    int debug_stall;
+};
+
+// ---------------------------------------------------------------- device side
+
+__device__ __forceinline__ void report(const Params &p, int code, int role, int iter)
+{
+    if (atomicCAS(p.status, 0, code) == 0) {
+        p.status[1] = role;
+        p.status[2] = int(blockIdx.x);
+        p.status[3] = iter;
+    }
+}
+
+// Bounded wait for the phase of parity `parity` of `bar`.  Returns false when
+// the CTA has aborted (if honour_abort) or when the watchdog expires; the
+// latter is recorded and raises the CTA's abort flag.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Params &p, volatile int *abort,
+                                      int role, int iter, bool honour_abort = true)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    uint32_t spins = 0;
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++spins & 15u) == 0) {
+            if (honour_abort && *abort) return false;
+            if (globaltimer() - t0 > p.watchdog_ns) {
+                *abort = 1;
+                report(p, kErrTimeout, role, iter);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tile_coords(const Params &p, int t, int &m_blk, int &n_blk)
+{
+    const int group_tiles = p.group_m * p.tiles_n;
+    const int g = t / group_tiles;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.group_m, p.tiles_m - first_m);
+    const int r = t - g * group_tiles;
+    m_blk = first_m + r % gm;
+    n_blk = r / gm;
+}
+
+// Shared-memory matrix descriptor of a K-major swizzled operand tile starting
+// at shared address `addr` (bits 0-13: address >> 4; 16-29: leading byte
+// offset >> 4; 32-45: stride byte offset >> 4; 46: version 1; 61-63: swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, const Params &p)
+{
+    const uint32_t lo = ((addr >> 4) & 0x3FFFu) | p.desc_lo_flags;
+    return (uint64_t(p.desc_hi) << 32) | lo;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constant__ Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = (kSmemAlign - (raw & (kSmemAlign - 1))) & (kSmemAlign - 1);
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+    const uint32_t sA = sbase + p.off_a;
+    const uint32_t sB = sbase + p.off_b;
+    const uint32_t sC = sbase + p.off_c;
+    const int S = p.stages;
+    const uint32_t bars = sbase + p.off_bar;
+    auto full = [&](int s) { return bars + 8u * uint32_t(s); };
+    auto empty = [&](int s) { return bars + 8u * uint32_t(S + s); };
+    auto acc_full = [&](int a) { return bars + 8u * uint32_t(2 * S + a); };
+    auto acc_empty = [&](int a) { return bars + 8u * uint32_t(2 * S + 2 + a); };
+    const uint32_t drain = bars + 8u * uint32_t(2 * S + 4);
+    const uint32_t stall = bars + 8u * uint32_t(2 * S + 5);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bar + 8u * uint32_t(2 * S + 6));
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = int(threadIdx.x) / 32;
+    const int lane = int(threadIdx.x) % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full(a), 1);
+            mbar_init(acc_empty(a), kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        mbar_init(stall, 1);
+        *abort = 0;
+        fence_mbar_init();
+        if (p.num_kb > 0) {
+            prefetch_tmap(&p.tmA);
+            prefetch_tmap(&p.tmB);
+        }
+        prefetch_tmap(&p.tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), uint32_t(p.tmem_cols));
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer: fill the ring, num_stages slots ahead
+            int s = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(p, t, mb, nb);
+                const int m0 = mb * p.bm, n0 = nb * p.bn;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(empty(s), ph ^ 1u, p, abort, 0, issued)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full(s), p.stage_tx);
+                    tma_load_2d(sA + uint32_t(s) * p.a_slot, &p.tmA, kb * p.bk, m0, full(s));
+                    tma_load_2d(sB + uint32_t(s) * p.b_slot, &p.tmB, kb * p.bk, n0, full(s));
+                    ++issued;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let the loads still in flight land before the CTA may exit:
+                // only the last min(S, issued) slots can be outstanding.
+                const int first = issued > S ? issued - S : 0;
+                for (int j = first; j < issued; ++j)
+                    wait_bar(full(j % S), uint32_t((j / S) & 1), p, abort, 0, j, false);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer: one thread drives the tensor core
+            int s = 0;
+            uint32_t ph = 0;
+            int a = 0;
+            uint32_t aph = 0;
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                if (!wait_bar(acc_empty(a), aph ^ 1u, p, abort, 1, it)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + uint32_t(a * p.acc_cols);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (p.debug_stall && it == 0) {
+                        // Test hook: a barrier nothing arrives on.
+                        if (!wait_bar(stall, 0, p, abort, 1, it)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!wait_bar(full(s), ph, p, abort, 1, it)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = sA + uint32_t(s) * p.a_slot;
+                    const uint32_t b_base = sB + uint32_t(s) * p.b_slot;
+                    for (int kk = 0; kk < p.n_kstep; ++kk) {
+                        const uint64_t bdesc = smem_desc(b_base + uint32_t(kk) * 32u, p);
+                        for (int h = 0; h < p.m_halves; ++h) {
+                            const uint64_t adesc =
+                                smem_desc(a_base + uint32_t(h) * 128u * p.row_bytes + uint32_t(kk) * 32u, p);
+                            mma_f16(d + uint32_t(h * p.bn), adesc, bdesc, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(empty(s));  // slot s may be refilled once these MMAs finish
+                    ++it;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(acc_full(a));  // accumulator a is complete
+                if (++a == p.acc_stages) {
+                    a = 0;
+                    aph ^= 1u;
+                }
+            }
+            // Every MMA this thread issued must finish before TMEM is freed.
+            mma_commit(drain);
+            wait_bar(drain, 0, p, abort, 1, it, false);
+        }
+    } else {
+        // ---------------- epilogue: 4 warps, warp w reads TMEM lanes 32*(w%4)..+31
+        const int q = warp & 3;
+        const uint32_t lane_base = uint32_t(q * 32) << 16;
+        const uint32_t my_bufs = sC + uint32_t((warp - 2) * kEpiBufs) * p.c_buf_bytes;
+        int a = 0;
+        uint32_t aph = 0;
+        uint32_t chunk = 0;
+        int tiles_done = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tiles_done) {
+            int mb, nb;
+            tile_coords(p, t, mb, nb);
+            const int m0 = mb * p.bm, n0 = nb * p.bn;
+            int ok = 1;
+            if (lane == 0) ok = wait_bar(acc_full(a), aph, p, abort, 2, tiles_done) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            for (int h = 0; h < p.m_halves; ++h) {
+                const int row0 = m0 + h * 128 + q * 32;
+                if (row0 >= p.M) continue;  // warp-uniform
+                for (int c = 0; c * kEpiCols < p.bn; ++c) {
+                    const int col0 = n0 + c * kEpiCols;
+                    if (col0 >= p.N) break;  // warp-uniform
+                    uint32_t v[32];
+                    if (p.num_kb > 0) {
+                        tmem_ld_32x32b_x32(tmem + lane_base + uint32_t(a * p.acc_cols + h * p.bn + c * kEpiCols), v);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;  // empty reduction
+                    }
+                    const uint32_t buf = my_bufs + (chunk & 1u) * p.c_buf_bytes;
+                    if (chunk >= 2 && lane == 0) bulk_wait_read<1>();  // buffer's previous store has read it
+                    __syncwarp();
+                    if (p.out_mode == 0) {
+                        // fp32: 128-byte rows, 128-byte swizzle (16-byte chunk j of row r at j ^ (r % 8))
+                        const uint32_t row = buf + uint32_t(lane) * 128u;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(row + (uint32_t(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                         v[4 * j + 3]);
+                    } else {
+                        // 16-bit: 64-byte rows, 64-byte swizzle (chunk j of row r at j ^ ((r / 2) % 4))
+                        const uint32_t row = buf + uint32_t(lane) * 64u;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float x0 = __uint_as_float(v[8 * j + 2 * e]);
+                                const float x1 = __uint_as_float(v[8 * j + 2 * e + 1]);
+                                if (p.out_mode == 1) {
+                                    __half2 h2 = __floats2half2_rn(x0, x1);
+                                    w[e] = *reinterpret_cast<uint32_t *>(&h2);
+                                } else {
+                                    __nv_bfloat162 b2 = __floats2bfloat162_rn(x0, x1);
+                                    w[e] = *reinterpret_cast<uint32_t *>(&b2);
+                                }
+                            }
+                            st_shared_v4(row + (uint32_t(j ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmC, col0, row0, buf);
+                        bulk_commit();
+                    }
+                    ++chunk;
+                }
+            }
+            // All TMEM reads of accumulator a are done: hand it back to the MMA warp.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(a));
+            if (++a == p.acc_stages) {
+                a = 0;
+                aph ^= 1u;
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, uint32_t(p.tmem_cols));
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+static CUtensorMapSwizzle swizzle_for(int row_bytes)
+{
+    return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+           : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                             : CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
+// Descriptor swizzle field (bits 61-63): 128 B -> 2, 64 B -> 4, 32 B -> 6.
+static uint32_t desc_layout_for(int row_bytes) { return row_bytes == 128 ? 2u : row_bytes == 64 ? 4u : 6u; }
+
+static CUtensorMapDataType tmap_dtype(int dt)
+{
+    return dt == kF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+           : dt == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+static int encode_2d(CUtensorMap *m, int dt, const void *base, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+                     uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz, CUtensorMapL2promotion l2)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return kErrCuda;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, tmap_dtype(dt), 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? kOk : kErrCuda;
+}
+
+}  // namespace tg
+
+using namespace tg;
+
+struct tgemm_plan_s {
+    int64_t M, N, K;
+    int dtype, out_dtype;
+    Layout L;
+    int device;
+    int num_sms;
+    int smem_limit;
+    int smem_launch;
+    int tiles_m, tiles_n, num_tiles, grid, group_m;
+    int *d_status;
+    unsigned long long watchdog_ns;
+    int debug_stall;
+    // tensor maps cached for the last pointer triple
+    const void *cA, *cB;
+    void *cC;
+    bool maps_valid;
+    Params params;
+};
+
+static const unsigned long long kDefaultWatchdogNs = 2000000000ull;
+
+static unsigned long long env_watchdog()
+{
+    const char *e = std::getenv("TGEMM_WATCHDOG_NS");
+    if (e && *e) {
+        char *end = nullptr;
+        unsigned long long v = std::strtoull(e, &end, 10);
+        if (end && *end == '\0' && v > 0) return v;
+    }
+    return kDefaultWatchdogNs;
+}
+
+extern "C" {
+
+int64_t tgemm_smem_bound(int dtype, int block_M, int block_N, int block_K, int num_stages)
+{
+    if (dtype != kF16 && dtype != kBF16) return -kErrUnsupportedDtype;
+    if (block_M <= 0 || block_N <= 0 || block_K <= 0 || num_stages <= 0) return -kErrInvalidArg;
+    return int64_t(num_stages) * (int64_t(block_M) * block_K + int64_t(block_K) * block_N) * dtype_bytes(dtype);
+}
+
+int64_t tgemm_smem_bytes(int dtype, int out_dtype, int block_M, int block_N, int block_K, int num_stages)
+{
+    if (dtype != kF16 && dtype != kBF16) return -kErrUnsupportedDtype;
+    if (out_dtype != kF32 && out_dtype != dtype) return -kErrUnsupportedDtype;
+    if (!tile_supported(block_M, block_N, block_K, dtype_bytes(dtype))) return -kErrNoKernel;
+    if (num_stages < 1 || num_stages > 64) return -kErrInvalidArg;
+    return int64_t(make_layout(block_M, block_N, block_K, num_stages, dtype, out_dtype).total);
+}
+
+int tgemm_smem_limit(void)
+{
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -kErrCuda;
+    }
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -kErrCuda;
+    }
+    return v;
+}
+
+int tgemm_validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N, int block_K,
+                   int num_stages, int64_t smem_limit)
+{
+    return validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit);
+}
+
+int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N,
+               int block_K, int num_stages)
+{
+    if (!out) return kErrInvalidArg;
+    *out = nullptr;
+    // Argument checks that need no device come first.
+    int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX);
+    if (rc != kOk) return rc;
+    int dev = 0, major = 0, minor = 0, sms = 0, limit = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ||
+        cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ||
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) {
+        cudaGetLastError();
+        return kErrCuda;
+    }
+    if (major != 10 || minor != 3) return kErrArch;
+    rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit);
+    if (rc != kOk) return rc;
+
+    tgemm_plan_s *p = new (std::nothrow) tgemm_plan_s();
+    if (!p) return kErrCuda;
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->dtype = dtype;
+    p->out_dtype = out_dtype;
+    p->L = make_layout(block_M, block_N, block_K, num_stages, dtype, out_dtype);
+    p->device = dev;
+    p->num_sms = sms;
+    p->smem_limit = limit;
+    // Request more than half of the SM's shared memory so that exactly one
+    // CTA is resident per SM: the persistent schedule and the TMEM allocation
+    // (up to all 512 columns) both assume it.
+    int one_per_sm = per_sm / 2 + 1;
+    p->smem_launch = int(p->L.total) > one_per_sm ? int(p->L.total) : one_per_sm;
+    if (p->smem_launch > limit) p->smem_launch = limit;
+    p->tiles_m = int((M + block_M - 1) / block_M);
+    p->tiles_n = int((N + block_N - 1) / block_N);
+    p->num_tiles = p->tiles_m * p->tiles_n;
+    p->grid = p->num_tiles < sms ? p->num_tiles : sms;
+    p->group_m = 8;
+    p->watchdog_ns = env_watchdog();
+    p->debug_stall = 0;
+    p->maps_valid = false;
+    if (cudaMalloc(&p->d_status, 4 * sizeof(int)) != cudaSuccess ||
+        cudaMemset(p->d_status, 0, 4 * sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        if (p->d_status) cudaFree(p->d_status);
+        delete p;
+        return kErrCuda;
+    }
+    if (cudaFuncSetAttribute(tgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_launch) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->d_status);
+        delete p;
+        return kErrCuda;
+    }
+
+    Params &q = p->params;
+    std::memset(&q, 0, sizeof(q));
+    const Layout &L = p->L;
+    q.M = int(M);
+    q.N = int(N);
+    q.K = int(K);
+    q.num_kb = int((K + block_K - 1) / block_K);
+    q.tiles_m = p->tiles_m;
+    q.tiles_n = p->tiles_n;
+    q.num_tiles = p->num_tiles;
+    q.group_m = p->group_m;
+    q.bm = block_M;
+    q.bn = block_N;
+    q.bk = block_K;
+    q.stages = num_stages;
+    q.n_kstep = block_K * L.in_bytes / 32;  // one MMA consumes K = 16 elements = 32 bytes
+    q.m_halves = L.m_halves;
+    q.out_mode = out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
+    q.acc_stages = L.acc_stages;
+    q.acc_cols = L.acc_cols;
+    q.tmem_cols = L.tmem_cols;
+    // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
+    // format (bits 7-9, 10-12: 0 fp16, 1 bf16), both K-major (bits 15, 16 =
+    // 0), N >> 3 (bits 17-22), M >> 4 (bits 24-28) with M = 128.
+    const uint32_t ab = dtype == kBF16 ? 1u : 0u;
+    q.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(block_N >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    q.a_slot = round_up(L.a_stage_bytes, kSmemAlign);
+    q.b_slot = round_up(L.b_stage_bytes, kSmemAlign);
+    q.stage_tx = L.a_stage_bytes + L.b_stage_bytes;
+    q.row_bytes = uint32_t(L.swizzle_bytes);
+    q.off_a = L.off_a;
+    q.off_b = L.off_b;
+    q.off_c = L.off_c;
+    q.off_bar = L.off_bar;
+    q.c_buf_bytes = L.c_buf_bytes;
+    // Leading byte offset is unused for swizzled K-major tiles whose K extent
+    // per MMA lies inside one swizzle row; encode 16 bytes.  Stride byte
+    // offset: 8 rows of one swizzle span each.
+    q.desc_lo_flags = (1u << 16);
+    const uint32_t sbo = 8u * uint32_t(L.swizzle_bytes);
+    q.desc_hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (desc_layout_for(L.swizzle_bytes) << 29);
+    q.watchdog_ns = p->watchdog_ns;
+    q.status = p->d_status;
+    q.debug_stall = 0;
+    *out = p;
+    return kOk;
+}
+
+static int aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+static int prepare_maps(tgemm_plan_s *p, const void *A, const void *B, void *C)
+{
+    if (p->maps_valid && p->cA == A && p->cB == B && p->cC == C) return kOk;
+    Params &q = p->params;
+    const Layout &L = p->L;
+    int rc = kOk;
+    if (p->K > 0) {
+        CUtensorMapSwizzle swz = swizzle_for(L.swizzle_bytes);
+        rc = encode_2d(&q.tmA, p->dtype, A, uint64_t(p->K), uint64_t(p->M), uint64_t(p->K) * L.in_bytes,
+                       uint32_t(L.bk), uint32_t(L.bm), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        if (rc == kOk)
+            rc = encode_2d(&q.tmB, p->dtype, B, uint64_t(p->K), uint64_t(p->N), uint64_t(p->K) * L.in_bytes,
+                           uint32_t(L.bk), uint32_t(L.bn), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    }
+    if (rc == kOk)
+        rc = encode_2d(&q.tmC, p->out_dtype, C, uint64_t(p->N), uint64_t(p->M), uint64_t(p->N) * L.out_bytes,
+                       uint32_t(kEpiCols), 32u, L.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                       CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (rc != kOk) {
+        p->maps_valid = false;
+        return rc;
+    }
+    p->cA = A;
+    p->cB = B;
+    p->cC = C;
+    p->maps_valid = true;
+    return kOk;
+}
+
+int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_stream_t stream)
+{
+    if (!p) return kErrInvalidArg;
+    if (p->M == 0 || p->N == 0) return kOk;  // empty product: nothing to write
+    if (!C || (p->K > 0 && (!A || !B))) return kErrInvalidArg;
+    if (!aligned16(C) || (p->K > 0 && (!aligned16(A) || !aligned16(B)))) return kErrAlignment;
+    int rc = prepare_maps(p, A, B, C);
+    if (rc != kOk) return rc;
+    p->params.watchdog_ns = p->watchdog_ns;
+    p->params.debug_stall = p->debug_stall;
+    tgemm_kernel<<<p->grid, kThreads, p->smem_launch, reinterpret_cast<cudaStream_t>(stream)>>>(p->params);
+    if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+    return kOk;
+}
+
+int tgemm_run_host(tgemm_plan_t p, const void *hA, const void *hB, void *hC, void *dA, void *dB, void *dC,
+                   tgemm_stream_t stream)
+{
+    if (!p) return kErrInvalidArg;
+    if (p->M == 0 || p->N == 0) return kOk;
+    if (!hC || !dC || (p->K > 0 && (!hA || !hB || !dA || !dB))) return kErrInvalidArg;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t a_bytes = size_t(p->M) * size_t(p->K) * p->L.in_bytes;
+    const size_t b_bytes = size_t(p->N) * size_t(p->K) * p->L.in_bytes;
+    const size_t c_bytes = size_t(p->M) * size_t(p->N) * p->L.out_bytes;
+    if (p->K > 0) {
+        if (cudaMemcpyAsync(dA, hA, a_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(dB, hB, b_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+            cudaGetLastError();
+            return kErrCuda;
+        }
+    }
+    int rc = tgemm_run(p, dA, dB, dC, stream);
+    if (rc != kOk) return rc;
+    if (cudaMemcpyAsync(hC, dC, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        cudaGetLastError();
+        return kErrCuda;
+    }
+    return kOk;
+}
+
+int tgemm_status(tgemm_plan_t p, int *detail)
+{
+    if (!p) return kErrInvalidArg;
+    int h[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(h, p->d_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(p->d_status, 0, sizeof(h)) != cudaSuccess) {
+        cudaGetLastError();
+        return -kErrCuda;
+    }
+    if (detail) std::memcpy(detail, h, sizeof(h));
+    return h[0];
+}
+
+int tgemm_set_watchdog_ns(tgemm_plan_t p, uint64_t ns)
+{
+    if (!p) return kErrInvalidArg;
+    p->watchdog_ns = ns ? (unsigned long long)ns : env_watchdog();
+    return kOk;
+}
+
+int tgemm_debug_stall(tgemm_plan_t p, int on)
+{
+    if (!p) return kErrInvalidArg;
+    p->debug_stall = on ? 1 : 0;
+    return kOk;
+}
+
+int tgemm_get_plan_info(tgemm_plan_t p, tgemm_plan_info *info)
+{
+    if (!p || !info) return kErrInvalidArg;
+    info->M = p->M;
+    info->N = p->N;
+    info->K = p->K;
+    info->dtype = p->dtype;
+    info->out_dtype = p->out_dtype;
+    info->block_M = p->L.bm;
+    info->block_N = p->L.bn;
+    info->block_K = p->L.bk;
+    info->num_stages = p->L.stages;
+    info->tiles_m = p->tiles_m;
+    info->tiles_n = p->tiles_n;
+    info->num_tiles = p->num_tiles;
+    info->grid = p->grid;
+    info->threads = kThreads;
+    info->num_k_blocks = p->params.num_kb;
+    info->acc_stages = p->L.acc_stages;
+    info->tmem_columns = p->L.tmem_cols;
+    info->smem_bytes = p->smem_launch;
+    info->smem_bound = p->L.bound;
+    info->smem_limit = p->smem_limit;
+    info->num_sms = p->num_sms;
+    return kOk;
+}
+
+int tgemm_destroy(tgemm_plan_t p)
+{
+    if (!p) return kOk;
+    int rc = kOk;
+    if (p->d_status && cudaFree(p->d_status) != cudaSuccess) {
+        cudaGetLastError();
+        rc = kErrCuda;
+    }
+    delete p;
+    return rc;
+}
+
+const char *tgemm_strerror(int code)
+{
+    switch (code < 0 ? -code : code) {
+    case kOk: return "ok";
+    case kErrInvalidArg: return "invalid argument";
+    case kErrUnsupportedDtype: return "unsupported dtype (operands fp16/bf16; output fp32 or the operand dtype)";
+    case kErrAlignment: return "pointer or row pitch not a multiple of 16 bytes";
+    case kErrSmemBudget: return "num_stages x (A tile + B tile) exceeds the per-block shared-memory limit";
+    case kErrNoKernel: return "tile shape not implemented (block_M 128/256, block_N 32..256 step 32, block_K 16/32/64)";
+    case kErrArch: return "device is not compute capability 10.3 (GB300)";
+    case kErrCuda: return "CUDA runtime or driver call failed";
+    case kErrTimeout: return "a pipeline wait in the kernel exceeded the watchdog limit";
+    default: return "unknown status code";
+    }
+}
+
+}  // extern "C"

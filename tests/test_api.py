@@ -1,0 +1,159 @@
+"""Host-side tests of the C ABI: loading, exports, validation, budget.
+
+No kernel is launched and no GPU is needed: these call only the functions
+that are pure host logic, plus tgemm_plan on a machine without a device
+(which must fail with a status, not crash).
+"""
+
+import itertools
+import os
+import re
+
+import pytest
+import torch
+
+import oracle
+import software_pipelined_tiled_02_gb300 as tg
+from software_pipelined_tiled_02_gb300 import build as tbuild
+from tests.conftest import ROOT, golden_lines
+
+LIMIT_227K = 227 * 1024  # cudaDevAttrMaxSharedMemoryPerBlockOptin on sm_100/sm_103
+PAGES_BUDGET = 228 * 1024
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tbuild.build()
+    return tg.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "tgemm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tgemm_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function(lib):
+    declared = header_functions()
+    assert len(declared) >= 13
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/tgemm.h but not exported"
+    assert sorted(tg.SYMBOLS) == declared
+
+
+def test_strerror_covers_every_code(lib):
+    texts = {tg.strerror(c) for c in range(9)}
+    assert len(texts) == 9
+    assert tg.strerror(99) == "unknown status code"
+    assert tg.strerror(-tg.ERR_CUDA) == tg.strerror(tg.ERR_CUDA)
+
+
+def test_smem_bound_matches_oracle_and_pages(lib):
+    # The library's bound and the oracle's are separate code; the pages'
+    # printed values pin both.
+    for t in golden_lines("smem_budget.txt"):
+        if t[0] == "tile":
+            bm, bn, bk, eb, per, _ = map(int, t[1:])
+            assert tg.tgemm_smem_bound(tg.F16, bm, bn, bk, 1) == per
+    for bm, bn, bk, s in itertools.product((64, 128, 256), (32, 64, 128, 256), (16, 32, 64), (1, 2, 3, 4, 6, 8)):
+        for dt in (tg.F16, tg.BF16):
+            assert tg.tgemm_smem_bound(dt, bm, bn, bk, s) == oracle.smem_bound(bm, bn, bk, s, 2)
+
+
+def test_smem_bytes_cover_the_bound(lib):
+    for bm, bn, bk, s in itertools.product((128, 256), (32, 64, 96, 128, 256), (16, 32, 64), (1, 2, 3, 4, 6)):
+        for out in (tg.F16, tg.F32):
+            b = tg.tgemm_smem_bytes(tg.F16, out, bm, bn, bk, s)
+            assert b >= tg.tgemm_smem_bound(tg.F16, bm, bn, bk, s)
+            assert b % 16 == 0 or b > 0
+
+
+def test_over_budget_config_rejected(lib):
+    # 256x256x64 at num_stages = 4 needs 256 KiB (chapter 11 section 4.5): it
+    # must be rejected before anything is launched, at the GB300 limit and at
+    # the pages' 228 KiB figure; 3 stages fit the bound.
+    for limit in (LIMIT_227K, PAGES_BUDGET):
+        assert tg.tgemm_validate(4000, 3000, 5000, tg.F16, tg.F32, 256, 256, 64, 4, limit) == tg.ERR_SMEM_BUDGET
+    assert tg.tgemm_smem_bound(tg.F16, 256, 256, 64, 3) <= LIMIT_227K
+
+
+def test_validate_rules(lib):
+    V = tg.tgemm_validate
+    L = LIMIT_227K
+    assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.OK
+    assert V(4096, 4096, 4096, tg.F16, tg.F16, 128, 256, 64, 4, L) == tg.OK
+    assert V(8192, 8192, 8192, tg.BF16, tg.BF16, 128, 256, 64, 4, L) == tg.OK
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 128, 64, 6, L) == tg.OK
+    # dtypes
+    assert V(128, 128, 128, tg.F32, tg.F32, 128, 128, 32, 3, L) == tg.ERR_UNSUPPORTED_DTYPE
+    assert V(128, 128, 128, tg.F16, tg.BF16, 128, 128, 32, 3, L) == tg.ERR_UNSUPPORTED_DTYPE
+    assert V(128, 128, 128, 7, tg.F32, 128, 128, 32, 3, L) == tg.ERR_UNSUPPORTED_DTYPE
+    # sizes and depth
+    assert V(-1, 128, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
+    assert V(128, 128, -8, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
+    assert V(2 ** 31, 128, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
+    assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 0, L) == tg.ERR_INVALID_ARG
+    # empty products and the empty reduction are valid
+    assert V(0, 128, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.OK
+    assert V(128, 0, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.OK
+    assert V(128, 128, 0, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.OK
+    # row pitch must be 16-byte aligned for the TMA engine
+    assert V(128, 128, 12, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_ALIGNMENT
+    assert V(128, 130, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_ALIGNMENT
+    assert V(128, 132, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.OK      # 528-byte fp32 rows
+    assert V(128, 132, 128, tg.F16, tg.F16, 128, 128, 32, 3, L) == tg.ERR_ALIGNMENT  # 264-byte fp16 rows
+    # tile shapes the kernel implements
+    assert V(128, 128, 128, tg.F16, tg.F32, 64, 128, 32, 3, L) == tg.ERR_NO_KERNEL
+    assert V(128, 128, 128, tg.F16, tg.F32, 128, 48, 32, 3, L) == tg.ERR_NO_KERNEL
+    assert V(128, 128, 128, tg.F16, tg.F32, 128, 512, 32, 3, L) == tg.ERR_NO_KERNEL
+    assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 128, 1, L) == tg.ERR_NO_KERNEL
+    assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 8, 3, L) == tg.ERR_NO_KERNEL
+    # depth is bounded only by the budget
+    assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 12, L) == tg.OK
+    assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 14, L) == tg.ERR_SMEM_BUDGET
+    assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 10 ** 6, L) == tg.ERR_SMEM_BUDGET
+
+
+def test_budget_rule_agrees_with_oracle_over_the_grid(lib):
+    # Whatever the real footprint adds, a config whose pages' bound exceeds
+    # the limit is always rejected, and the rejection is monotone in depth.
+    for bm, bn, bk in itertools.product((128, 256), (64, 128, 256), (16, 32, 64)):
+        prev_ok = True
+        for s in range(1, 16):
+            rc = tg.tgemm_validate(4096, 4096, 4096, tg.F16, tg.F16, bm, bn, bk, s, LIMIT_227K)
+            if oracle.smem_bound(bm, bn, bk, s, 2) > LIMIT_227K:
+                assert rc == tg.ERR_SMEM_BUDGET
+            assert rc in (tg.OK, tg.ERR_SMEM_BUDGET)
+            if not prev_ok:
+                assert rc == tg.ERR_SMEM_BUDGET
+            prev_ok = rc == tg.OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_plan_without_device_fails_cleanly(lib):
+    rc, h = tg.tgemm_plan(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 3)
+    assert rc == tg.ERR_CUDA and h is None
+    # argument errors are reported before any device query
+    rc, h = tg.tgemm_plan(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 0)
+    assert rc == tg.ERR_INVALID_ARG and h is None
+    rc, h = tg.tgemm_plan(128, 128, 128, tg.F16, tg.F32, 64, 128, 32, 2)
+    assert rc == tg.ERR_NO_KERNEL and h is None
+    assert tg.tgemm_smem_limit() < 0
+    assert tg.tgemm_destroy(None) == tg.OK
+
+
+def test_null_plan_arguments(lib):
+    assert lib.tgemm_run(None, None, None, None, None) == tg.ERR_INVALID_ARG
+    assert lib.tgemm_status(None, None) == tg.ERR_INVALID_ARG
+    assert lib.tgemm_get_plan_info(None, None) == tg.ERR_INVALID_ARG
+    assert lib.tgemm_plan(None, 1, 1, 8, 0, 2, 128, 128, 32, 1) == tg.ERR_INVALID_ARG
+
+
+def test_missing_library_raises(tmp_path):
+    with pytest.raises(RuntimeError):
+        tg._lib_saved = tg._lib
+        tg._lib = None
+        try:
+            tg.load(str(tmp_path / "nope.so"))
+        finally:
+            tg._lib = tg._lib_saved

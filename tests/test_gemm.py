@@ -1,0 +1,211 @@
+"""GPU parity: the sm_103a kernel against the CPU oracle, element by element.
+
+Acceptance (oracle.check): |C - R| <= 1e-4 * S + 1e-5 (+ one output ulp for
+16-bit output) and the pages' rtol = atol = 1e-2; integer-valued inputs must
+match exactly.  Small problems are compared in full; the full-size workloads
+are compared on sampled entries (whole first/last rows and columns plus
+random entries) that the oracle computes one by one, in the launch
+configuration the benchmark times.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from software_pipelined_tiled_02_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def to_dev(bits, dtype):
+    return inputs.bits_to_torch(bits, dtype).cuda()
+
+
+def run(tg, A, B, dtype, out, block, stages):
+    M, K = A.shape
+    N = B.shape[0]
+    plan = tg.Plan(M, N, K, dtype, out, block, stages)
+    dA, dB = to_dev(A, dtype), to_dev(B, dtype)
+    C = torch.full((M, N), float("nan"), dtype=TORCH[out], device="cuda")
+    plan.run(dA, dB, C)
+    torch.cuda.synchronize()
+    rc, detail = plan.status()
+    assert rc == 0, f"kernel status {rc} {detail}"
+    plan.close()
+    return C
+
+
+def as_f64(C):
+    return C.float().cpu().double().numpy()
+
+
+def assert_close(C, R, S, out):
+    ok, worst, idx = oracle.check(C, R, S, out)
+    assert ok, f"worst error/bound {worst:.3g} at flat index {idx}: got {np.ravel(C)[idx]!r} want {np.ravel(R)[idx]!r}"
+
+
+# ------------------------------------------------------------ small, full compare
+
+def test_gemm_128_f16_uniform_tile_128x128x32_s3(cuda_lib):
+    w = inputs.WORKLOADS["gemm_128_f16_uniform"]
+    A, B = inputs.workload_operands("gemm_128_f16_uniform")
+    C = as_f64(run(cuda_lib, A, B, "f16", "f32", w["tile"], w["stages"]))
+    R, S = oracle.gemm(A, B, "f16")
+    assert_close(C, R, S, "f32")
+
+
+CONFIGS = [
+    ((128, 128, 32), 3),
+    ((128, 256, 64), 4),
+    ((256, 128, 64), 3),
+    ((128, 64, 16), 2),
+    ((128, 96, 32), 1),
+    ((256, 256, 64), 3),
+    ((128, 32, 64), 5),
+]
+SHAPES = [(300, 200, 136), (257, 96, 72), (129, 264, 1032), (1, 32, 8), (64, 512, 16)]
+
+
+@pytest.mark.parametrize("block,stages", CONFIGS, ids=lambda v: str(v))
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("bf16", "bf16"), ("f16", "f16"), ("bf16", "f32")])
+def test_small_shapes_all_tiles(cuda_lib, block, stages, shape, dtype, out):
+    M, N, K = shape
+    A, B = inputs.operands(100 + M + N + K, M, N, K, dtype, "uniform")
+    C = as_f64(run(cuda_lib, A, B, dtype, out, block, stages))
+    R, S = oracle.gemm(A, B, dtype)
+    assert_close(C, R, S, out)
+
+
+@pytest.mark.parametrize("block,stages", CONFIGS, ids=lambda v: str(v))
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_integer_inputs_bit_exact(cuda_lib, block, stages, dtype):
+    M, N, K = 300, 520, 2056
+    A, B = inputs.operands(40, M, N, K, dtype, "int", lo=-4, hi=4)
+    C = as_f64(run(cuda_lib, A, B, dtype, "f32", block, stages))
+    R, _ = oracle.gemm(A, B, dtype)
+    assert np.array_equal(C, R)
+
+
+# ------------------------------------------------------------ degenerate cases
+
+def test_empty_product_is_a_noop(cuda_lib):
+    for M, N in ((0, 64), (64, 0)):
+        plan = cuda_lib.Plan(M, N, 64, "f16", "f32", (128, 128, 32), 3)
+        A = torch.zeros((M, 64), dtype=torch.float16, device="cuda")
+        B = torch.zeros((N, 64), dtype=torch.float16, device="cuda")
+        C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+        plan.run(A, B, C)
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+
+
+@pytest.mark.parametrize("out", ["f32", "f16"])
+def test_empty_reduction_gives_zeros(cuda_lib, out):
+    M, N = 200, 136
+    plan = cuda_lib.Plan(M, N, 0, "f16", out, (128, 128, 32), 3)
+    A = torch.empty((M, 0), dtype=torch.float16, device="cuda")
+    B = torch.empty((N, 0), dtype=torch.float16, device="cuda")
+    C = torch.full((M, N), 7.0, dtype=TORCH[out], device="cuda")
+    plan.run(A, B, C)
+    torch.cuda.synchronize()
+    assert plan.status()[0] == 0
+    assert not C.any()
+
+
+def test_k_smaller_than_block_k(cuda_lib):
+    M, N, K = 130, 70 * 4, 8
+    A, B = inputs.operands(9, M, N, K, "f16", "uniform")
+    C = as_f64(run(cuda_lib, A, B, "f16", "f32", (128, 256, 64), 4))
+    R, S = oracle.gemm(A, B, "f16")
+    assert_close(C, R, S, "f32")
+
+
+def test_output_not_written_outside_c(cuda_lib):
+    # C is a view into a larger buffer: the guard bands around it must survive.
+    M, N, K = 200, 136, 64
+    A, B = inputs.operands(12, M, N, K, "f16", "uniform")
+    plan = cuda_lib.Plan(M, N, K, "f16", "f32", (128, 128, 32), 3)
+    big = torch.full((M + 64, N), -5.0, dtype=torch.float32, device="cuda")
+    C = big[32:32 + M]
+    plan.run(to_dev(A, "f16"), to_dev(B, "f16"), C)
+    torch.cuda.synchronize()
+    assert torch.all(big[:32] == -5.0) and torch.all(big[32 + M:] == -5.0)
+    R, S = oracle.gemm(A, B, "f16")
+    assert_close(as_f64(C), R, S, "f32")
+
+
+def test_plan_rejects_over_budget_on_device(cuda_lib):
+    rc, h = cuda_lib.tgemm_plan(4000, 3000, 5000, "f16", "f32", 256, 256, 64, 4)
+    assert rc == cuda_lib.ERR_SMEM_BUDGET and h is None
+    assert cuda_lib.tgemm_smem_limit() >= 200 * 1024
+
+
+def test_misaligned_pointer_rejected_before_launch(cuda_lib):
+    plan = cuda_lib.Plan(128, 128, 64, "f16", "f32", (128, 128, 32), 3)
+    A = torch.zeros(128 * 64 + 8, dtype=torch.float16, device="cuda")
+    B = torch.zeros((128, 64), dtype=torch.float16, device="cuda")
+    C = torch.zeros((128, 128), dtype=torch.float32, device="cuda")
+    rc = cuda_lib.tgemm_run(plan.handle, A.data_ptr() + 2, B.data_ptr(), C.data_ptr(), 0)
+    assert rc == cuda_lib.ERR_ALIGNMENT
+
+
+def test_run_host_end_to_end(cuda_lib):
+    M, N, K = 384, 256, 320
+    A, B = inputs.operands(21, M, N, K, "bf16", "normal")
+    plan = cuda_lib.Plan(M, N, K, "bf16", "bf16", (128, 128, 64), 4)
+    hA = inputs.bits_to_torch(A, "bf16").pin_memory()
+    hB = inputs.bits_to_torch(B, "bf16").pin_memory()
+    hC = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    dA = torch.empty_like(hA, device="cuda")
+    dB = torch.empty_like(hB, device="cuda")
+    dC = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    plan.run_host(hA, hB, hC, dA, dB, dC)
+    torch.cuda.synchronize()
+    assert plan.status()[0] == 0
+    R, S = oracle.gemm(A, B, "bf16")
+    assert_close(hC.float().double().numpy(), R, S, "bf16")
+
+
+# ------------------------------------------------------------ full-size workloads
+
+def sample_entries(M, N, n_random, seed):
+    rng = np.random.default_rng(seed)
+    rows = [np.zeros(N, np.int64), np.full(N, M - 1), np.arange(M), np.arange(M), rng.integers(0, M, n_random)]
+    cols = [np.arange(N), np.arange(N), np.zeros(M, np.int64), np.full(M, N - 1), rng.integers(0, N, n_random)]
+    return np.concatenate(rows), np.concatenate(cols)
+
+
+def full_size(cuda_lib, name, block=None, stages=None):
+    w = inputs.WORKLOADS[name]
+    A, B = inputs.workload_operands(name)
+    if block is None:
+        block, stages = cuda_lib.default_config(w["M"], w["N"], w["K"], w["dtype"], w["out"])
+    C = run(cuda_lib, A, B, w["dtype"], w["out"], block, stages)
+    return w, A, B, C
+
+
+@pytest.mark.parametrize("name", ["gemm_4096_f16_normal", "gemm_8192_bf16_normal"])
+def test_full_size_sampled(cuda_lib, name):
+    w, A, B, C = full_size(cuda_lib, name)
+    rows, cols = sample_entries(w["M"], w["N"], 8192, 5)
+    R, S = oracle.gemm_entries(A, B, w["dtype"], rows, cols)
+    got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+    assert_close(as_f64(got), R, S, w["out"])
+    assert torch.isfinite(C.float()).all()
+
+
+@pytest.mark.parametrize("name", ["gemm_512x512x32768_f16_uniform", "gemm_4000x3000x5000_f16_uniform"])
+def test_full_size_complete(cuda_lib, name):
+    w, A, B, C = full_size(cuda_lib, name)
+    R, S = oracle.gemm(A, B, w["dtype"])
+    assert_close(as_f64(C), R, S, w["out"])
+
+
+def test_long_k_integer_exact(cuda_lib):
+    w, A, B, C = full_size(cuda_lib, "gemm_512x512x32768_f16_int")
+    R, _ = oracle.gemm(A, B, w["dtype"])
+    assert np.array_equal(as_f64(C), R)

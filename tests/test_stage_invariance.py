@@ -1,0 +1,54 @@
+"""Bit-identity across num_stages at a fixed tile.
+
+Pipelining changes when data arrives, never what is summed or in which order
+(chapter 11 "Pipeline and autotuning", section 2.4: throughput, not the
+result).  The kernel's summation order depends only on the tile shape, so
+every depth must give the same bits, including the unpipelined num_stages=1.
+"""
+
+import pytest
+import torch
+
+from software_pipelined_tiled_02_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def bits(C):
+    return C.view(torch.int32 if C.element_size() == 4 else torch.int16)
+
+
+def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed):
+    A, B = inputs.operands(seed, M, N, K, dtype, "normal")
+    dA = inputs.bits_to_torch(A, dtype).cuda()
+    dB = inputs.bits_to_torch(B, dtype).cuda()
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[out]
+    res = []
+    for s in stage_list:
+        plan = tg.Plan(M, N, K, dtype, out, block, s)
+        C = torch.full((M, N), float("nan"), dtype=tdt, device="cuda")
+        plan.run(dA, dB, C)
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+        res.append(C)
+        plan.close()
+    return res
+
+
+@pytest.mark.parametrize("block,stage_list", [
+    ((128, 128, 32), (1, 2, 3, 4, 6)),
+    ((128, 256, 64), (1, 2, 3, 4)),
+    ((256, 128, 64), (1, 2, 3)),
+    ((128, 64, 16), (1, 2, 4, 8)),
+])
+@pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("bf16", "bf16")])
+def test_bit_identical_across_stages(cuda_lib, block, stage_list, dtype, out):
+    res = outputs_over_stages(cuda_lib, 1000, 1040, 2056, dtype, out, block, stage_list, seed=77)
+    for s, C in zip(stage_list[1:], res[1:]):
+        assert torch.equal(bits(C), bits(res[0])), f"num_stages={s} differs"
+
+
+def test_bit_identical_across_stages_4096(cuda_lib):
+    res = outputs_over_stages(cuda_lib, 4096, 4096, 4096, "f16", "f16", (128, 128, 32), (1, 2, 3, 4, 6), seed=2)
+    for C in res[1:]:
+        assert torch.equal(bits(C), bits(res[0]))
