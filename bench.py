@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Throughput of the pipelined tiled GEMM on GB300, one JSON line.
+
+A step is one C = A . B^T over the workload's seeded synthetic operands
+(default: 4096^3 fp16 normal, fp16 output: the headline GEMM TFLOP/s
+workload).  W untimed warm-up steps, then K timed steps; before every step
+a 256 MiB buffer is written so that L2 (129 MB) holds no operand; each
+step's kernel is bracketed by CUDA events on the launching stream and the
+region by a barrier and a device synchronise on both sides.
+
+Reported: value (TFLOP/s, 2*M*N*K per step / mean kernel time), an e2e
+figure through tgemm_run_host (pinned host operands copied in and the result
+copied out every step), the roofline of the kernel against the measured
+dense tensor peak, SM clocks sampled during the timed region, and the CPU
+oracle timed on a bounded sample of the same workload.
+
+``--impl reference`` times the CPU oracle instead (the reference arm).
+``--gpus N`` under torchrun runs N independent replicas (weak scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNK/t) at fp16 4096³ and % of GB300 dense tensor peak"
+FALLBACK_PEAK_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 * 1024 * 1024
+CSRC = os.path.join(ROOT, "software_pipelined_tiled_02_gb300", "csrc")
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="gemm_4096_f16_normal")
+    ap.add_argument("--block", default=None, help="bm,bn,bk (default: tuned table)")
+    ap.add_argument("--stages", type=int, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_max(values, dist, device):
+    """Elementwise max over ranks of a list of floats."""
+    if dist is None:
+        return list(values)
+    import torch
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def aggregate(per_rank_flops, max_seconds, world):
+    """Whole-job throughput (TFLOP/s): all ranks' work over the slowest rank's time."""
+    if max_seconds <= 0:
+        return 0.0
+    return per_rank_flops * world / max_seconds / 1e12
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(PROFILES, f"tgemm_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        return self.summary()
+
+    def summary(self):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(t=t, sm=float(parts[2]), smax=float(parts[3]), power=float(parts[4]),
+                                 active=parts[5], hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        inside = [r for r in rows if any(a - 0.15 <= r["t"] <= b + 0.15 for a, b in self.windows)]
+        use = inside or rows
+        reasons = set()
+        for r in use:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_max_mhz": max(r["smax"] for r in use),
+                "reasons": sorted(reasons), "samples": len(use), "in_timed_region": bool(inside),
+                "power_w_max": max(r["power"] for r in use)}
+
+
+# ------------------------------------------------------------------ arms
+
+def cpu_baseline(A, B, w, seconds):
+    """The oracle, as it stands, on whole rows of C until `seconds` elapse.
+
+    The operands are decoded to binary64 once before timing (they are
+    resident, as the GPU arm's operands are); the timed part is the oracle's
+    in-order fp64 sums."""
+    import oracle
+
+    M, N, K = w["M"], w["N"], w["K"]
+    oracle.build()
+    cores = oracle.num_threads()
+    Ad, Bd = oracle.decode(A, w["dtype"]), oracle.decode(B, w["dtype"])
+    chunk = max(cores, 16)
+    done, t0 = 0, time.perf_counter()
+    while done < M and time.perf_counter() - t0 < seconds:
+        n = min(chunk, M - done)
+        oracle.gemm_decoded_rows(Ad, Bd, done, n)
+        done += n
+    dt = time.perf_counter() - t0
+    flops = 2.0 * done * N * K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"rows 0..{done - 1} of C ({done}x{N}x{K} in-order fp64 multiply-adds, {dt:.1f} s, "
+                      f"operands decoded once beforehand) of the same seeded {w['dtype']} workload"}
+
+
+def run_reference(args, w, world, rank):
+    """Reference arm: the CPU oracle timed on bounded samples of the workload."""
+    if rank != 0:
+        return None
+    import oracle
+    from software_pipelined_tiled_02_gb300 import inputs
+
+    A, B = inputs.workload_operands(args.workload)
+    oracle.build()
+    cores = oracle.num_threads()
+    M, N, K = w["M"], w["N"], w["K"]
+    rows = min(M, max(16, cores))
+    Ad, Bd = oracle.decode(A, w["dtype"]), oracle.decode(B, w["dtype"])
+    for i in range(args.warmup):
+        oracle.gemm_decoded_rows(Ad, Bd, (i * rows) % (M - rows + 1), rows)
+    times = []
+    for i in range(args.steps):
+        r0 = (i * rows) % (M - rows + 1)
+        t0 = time.perf_counter()
+        oracle.gemm_decoded_rows(Ad, Bd, r0, rows)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    flops = 2.0 * rows * N * K
+    value = flops * len(times) / total / 1e12
+    sample = (f"{rows} rows of C per step ({rows}x{N}x{K} in-order fp64 multiply-adds, operands decoded once "
+              f"beforehand) of the seeded {w['dtype']} workload")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(args, w, None, None),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def config_block(args, w, block, stages):
+    cfg = {"workload": args.workload, "M": w["M"], "N": w["N"], "K": w["K"], "operand_dtype": w["dtype"],
+           "accumulate": "f32", "out_dtype": w["out"], "distribution": w["dist"], "seed": w["seed"],
+           "l2": "256 MiB buffer written before every timed step (L2 is 129 MB)"}
+    if block is not None:
+        cfg.update({"block_M": block[0], "block_N": block[1], "block_K": block[2], "num_stages": stages})
+    return cfg
+
+
+def run_ours(args, w, world, rank, local):
+    import torch
+
+    import software_pipelined_tiled_02_gb300 as tg
+    from software_pipelined_tiled_02_gb300 import inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    tg.load()
+    M, N, K = w["M"], w["N"], w["K"]
+    if args.block:
+        block = tuple(int(x) for x in args.block.split(","))
+        stages = args.stages or 4
+    else:
+        block, stages = tg.default_config(M, N, K, w["dtype"], w["out"])
+        if args.stages:
+            stages = args.stages
+    A, B = inputs.workload_operands(args.workload)
+    hA = inputs.bits_to_torch(A, w["dtype"])
+    hB = inputs.bits_to_torch(B, w["dtype"])
+    dA, dB = hA.to(dev), hB.to(dev)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[w["out"]]
+    dC = torch.empty((M, N), dtype=tdt, device=dev)
+    plan = tg.Plan(M, N, K, w["dtype"], w["out"], block, stages)
+    info = plan.info
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = 2.0 * M * N * K
+
+    sampler = None if args.no_clocks else ClockSampler(local)
+    if sampler:
+        sampler.start()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        plan.run(dA, dB, dC, stream)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        time.sleep(0.4)  # let the sampler start before the timed region
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        plan.run(dA, dB, dC, stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    t_wall1 = time.time()
+    if sampler:
+        sampler.mark(t_wall0, t_wall1)
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    code, detail = plan.status()
+    if code != tg.OK:
+        raise RuntimeError(f"kernel reported {tg.strerror(code)} {detail}")
+    mean_ms = sum(kernel_ms) / len(kernel_ms)
+    (max_mean_ms,) = reduce_max([mean_ms], dist, dev)
+    value = aggregate(flops, max_mean_ms / 1e3, world)
+
+    e2e = None
+    if not args.no_e2e:
+        pA, pB = hA.pin_memory(), hB.pin_memory()
+        pC = torch.empty((M, N), dtype=tdt).pin_memory()
+        for _ in range(3):
+            plan.run_host(pA, pB, pC, dA, dB, dC, stream)
+        torch.cuda.synchronize(dev)
+        e_steps = max(1, min(args.steps, 200))
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        tw0 = time.time()
+        for i in range(e_steps):
+            es[i].record(stream)
+            plan.run_host(pA, pB, pC, dA, dB, dC, stream)
+            ee[i].record(stream)
+        torch.cuda.synchronize(dev)
+        if sampler:
+            sampler.mark(tw0, time.time())
+        e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e_steps
+        (e_max,) = reduce_max([e_ms], dist, dev)
+        e2e = {"value": aggregate(flops, e_max / 1e3, world), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(pA.numel() * pA.element_size() + pB.numel() * pB.element_size()),
+               "d2h_bytes_per_step": int(pC.numel() * pC.element_size()), "steps": e_steps,
+               "ms_per_step": e_max, "path": "tgemm_run_host (pinned host A,B -> device; kernel; C -> pinned host)"}
+        if plan.status()[0] != tg.OK:
+            raise RuntimeError("kernel reported an error in the end-to-end leg")
+
+    clocks = sampler.stop() if sampler else None
+
+    peaks = measured_peaks()
+    if peaks and peaks.get("bf16_tflops"):
+        peak, peak_src = float(peaks["bf16_tflops"]), "measured"
+    else:
+        peak, peak_src = FALLBACK_PEAK_TFLOPS, "fallback"
+    achieved = flops / (mean_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": recorded_traffic(args.workload),
+                "peak_source": f"{peak_src} dense bf16 burst (fp16 runs at the bf16 rate: nominal ratio 1)",
+                "kernel": "tgemm_kernel", "flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": (M * K + N * K) * 2 + M * N * (4 if w["out"] == "f32" else 2)}
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(A, B, w, args.cpu_seconds)
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": max_mean_ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+                "config": config_block(args, w, block, stages), "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
+                "plan": {k: info[k] for k in ("grid", "num_tiles", "smem_bytes", "tmem_columns", "acc_stages")},
+                "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms), "max": max(kernel_ms)}}
+    plan.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return line
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from software_pipelined_tiled_02_gb300 import inputs
+
+    if args.workload not in inputs.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; one of {sorted(inputs.WORKLOADS)}")
+    if args.warmup < 3 and args.impl == "ours":
+        raise SystemExit("at least 3 warm-up steps are required")
+    w = inputs.WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, w, world, rank)
+    else:
+        line = run_ours(args, w, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

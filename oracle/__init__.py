@@ -67,6 +67,8 @@ def lib():
             L.oracle_gemm_entries.restype = ctypes.c_int
             L.oracle_gemm_rows.argtypes = [i64, i64, i64, p, p, ctypes.c_int, i64, i64, p]
             L.oracle_gemm_rows.restype = ctypes.c_int
+            L.oracle_gemm_decoded_rows.argtypes = [i64, i64, i64, p, p, i64, i64, p]
+            L.oracle_gemm_decoded_rows.restype = ctypes.c_int
             L.oracle_smem_bound.argtypes = [i64] * 5
             L.oracle_smem_bound.restype = i64
             L.oracle_max_stages.argtypes = [i64] * 5
@@ -150,6 +152,20 @@ def gemm_rows(A, B, dtype: str, row0: int, nrows: int) -> np.ndarray:
     rc = lib().oracle_gemm_rows(M, N, K, _ptr(A), _ptr(B), _DT[dtype], row0, nrows, _ptr(R))
     if rc != 0:
         raise RuntimeError("oracle_gemm_rows failed")
+    return R
+
+
+def gemm_decoded_rows(Ad, Bd, row0: int, nrows: int) -> np.ndarray:
+    """Rows ``[row0, row0 + nrows)`` of ``Ad . Bd^T`` for float64 operands
+    already produced by :func:`decode` (same sums, same order as :func:`gemm`)."""
+    Ad = np.ascontiguousarray(Ad, dtype=np.float64)
+    Bd = np.ascontiguousarray(Bd, dtype=np.float64)
+    M, K = Ad.shape
+    N, _ = Bd.shape
+    R = np.empty((nrows, N), dtype=np.float64)
+    rc = lib().oracle_gemm_decoded_rows(M, N, K, _ptr(Ad), _ptr(Bd), row0, nrows, _ptr(R))
+    if rc != 0:
+        raise RuntimeError("oracle_gemm_decoded_rows failed")
     return R
 
 

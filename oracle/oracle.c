@@ -241,6 +241,26 @@ int oracle_gemm_entries(int64_t M, int64_t N, int64_t K, const uint16_t *A, cons
     return fail ? -1 : 0;
 }
 
+/* The product of operands already decoded to binary64 (A: M x K, B: N x K
+ * row-major), rows [row0, row0 + nrows) only; R: nrows x N.  Same entries,
+ * same summation order as oracle_gemm.  Lets a timed sample of a large
+ * workload measure the sums with the operands resident, decoded once. */
+int oracle_gemm_decoded_rows(int64_t M, int64_t N, int64_t K, const double *Ad, const double *Bd,
+                             int64_t row0, int64_t nrows, double *R)
+{
+    if (M < 0 || N < 0 || K < 0 || row0 < 0 || nrows < 0 || row0 + nrows > M)
+        return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = row0; i < row0 + nrows; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double r, s;
+            dot(Ad + i * K, Bd + j * K, K, &r, &s);
+            R[(i - row0) * N + j] = r;
+        }
+    }
+    return 0;
+}
+
 /* Rows [row0, row0 + nrows) of the product, all N columns; used to time a
  * bounded sample of a large workload.  R: nrows x N. */
 int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B,

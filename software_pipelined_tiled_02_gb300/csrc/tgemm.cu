@@ -109,6 +109,19 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Param
     }
 }
 
+// Warp-collective form of wait_bar: every lane polls once (the common case
+// is a phase that has already completed); otherwise lane 0 waits with the
+// watchdog and the outcome is broadcast, so the warp stays converged and its
+// control flow uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Params &p, volatile int *abort,
+                                          int role, int iter, bool honour_abort = true)
+{
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    int ok = 1;
+    if ((threadIdx.x & 31u) == 0) ok = wait_bar(bar, parity, p, abort, role, iter, honour_abort) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ void tile_coords(const Params &p, int t, int &m_blk, int &n_blk)
 {
     const int group_tiles = p.group_m * p.tiles_n;
@@ -127,6 +140,86 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, const Params &p)
 {
     const uint32_t lo = ((addr >> 4) & 0x3FFFu) | p.desc_lo_flags;
     return (uint64_t(p.desc_hi) << 32) | lo;
+}
+
+struct MmaCtx {
+    uint32_t sA, sB, tmem, bars;
+    int S;
+    uint32_t stall, drain;
+};
+
+// The MMA warp's main loop.  NK = MMAs of K = 16 per ring slot (block_K / 16),
+// MH = MMAs of M = 128 per k-step (block_M / 128).  Descriptors of slot s are
+// the slot-0 descriptors plus s slot strides (address field in 16-byte units);
+// k-step kk adds 32 bytes, the second M-half adds 128 operand rows.
+template <int NK, int MH>
+__device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volatile int *abort, int lane)
+{
+    const int S = c.S;
+    auto full = [&](int s) { return c.bars + 8u * uint32_t(s); };
+    auto empty = [&](int s) { return c.bars + 8u * uint32_t(S + s); };
+    auto acc_full = [&](int a) { return c.bars + 8u * uint32_t(2 * S + a); };
+    auto acc_empty = [&](int a) { return c.bars + 8u * uint32_t(2 * S + 2 + a); };
+    const uint64_t ad0 = smem_desc(c.sA, p), bd0 = smem_desc(c.sB, p);
+    const uint64_t a_step = p.a_slot >> 4, b_step = p.b_slot >> 4;
+    const uint64_t a_half = (128u * p.row_bytes) >> 4;
+    const uint32_t idesc = p.idesc;
+    int s = 0;
+    uint32_t ph = 0;
+    uint64_t ad = ad0, bd = bd0;
+    int a = 0;
+    uint32_t aph = 0;
+    int it = 0;
+    bool ok = true;
+    if (p.debug_stall) ok = warp_wait(c.stall, 0, p, abort, 1, 0);  // test hook: nothing arrives
+    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        if (!warp_wait(acc_empty(a), aph ^ 1u, p, abort, 1, it)) break;
+        tc_fence_after();
+        const uint32_t d = c.tmem + uint32_t(a * p.acc_cols);
+        const uint32_t d2 = d + uint32_t(p.bn);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!warp_wait(full(s), ph, p, abort, 1, it)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t first = kb != 0 ? 1u : 0u;
+#pragma unroll
+                for (int kk = 0; kk < NK; ++kk) {
+#pragma unroll
+                    for (int h = 0; h < MH; ++h)
+                        mma_f16(h ? d2 : d, ad + uint64_t(2 * kk) + (h ? a_half : 0), bd + uint64_t(2 * kk), idesc,
+                                kk == 0 ? first : 1u);
+                }
+                mma_commit(empty(s));  // slot s may be refilled once these MMAs finish
+            }
+            __syncwarp();
+            ++it;
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+                ad = ad0;
+                bd = bd0;
+            } else {
+                ad += a_step;
+                bd += b_step;
+            }
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(acc_full(a));  // accumulator a is complete
+        __syncwarp();
+        if (++a == p.acc_stages) {
+            a = 0;
+            aph ^= 1u;
+        }
+    }
+    // Every MMA this warp issued must finish before TMEM is freed.
+    if (lane == 0) {
+        mma_commit(c.drain);
+        wait_bar(c.drain, 0, p, abort, 1, it, false);
+    }
+    __syncwarp();
 }
 
 __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constant__ Params p)
@@ -182,92 +275,54 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- producer: fill the ring, num_stages slots ahead
-            int s = 0;
-            uint32_t ph = 0;
-            int issued = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                int mb, nb;
-                tile_coords(p, t, mb, nb);
-                const int m0 = mb * p.bm, n0 = nb * p.bn;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(empty(s), ph ^ 1u, p, abort, 0, issued)) {
-                        ok = false;
-                        break;
-                    }
+        // ---------------- producer: fill the ring, up to num_stages slots ahead.
+        // The whole warp runs the loop (warp-uniform control); lane 0 issues.
+        int s = 0;
+        uint32_t ph = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            int mb, nb;
+            tile_coords(p, t, mb, nb);
+            const int m0 = mb * p.bm, n0 = nb * p.bn;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                if (!warp_wait(empty(s), ph ^ 1u, p, abort, 0, issued)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
                     mbar_arrive_expect_tx(full(s), p.stage_tx);
                     tma_load_2d(sA + uint32_t(s) * p.a_slot, &p.tmA, kb * p.bk, m0, full(s));
                     tma_load_2d(sB + uint32_t(s) * p.b_slot, &p.tmB, kb * p.bk, n0, full(s));
-                    ++issued;
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
                 }
-            }
-            if (!ok) {
-                // Let the loads still in flight land before the CTA may exit:
-                // only the last min(S, issued) slots can be outstanding.
-                const int first = issued > S ? issued - S : 0;
-                for (int j = first; j < issued; ++j)
-                    wait_bar(full(j % S), uint32_t((j / S) & 1), p, abort, 0, j, false);
+                __syncwarp();
+                ++issued;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
+        if (!ok && lane == 0) {
+            // Let the loads still in flight land before the CTA may exit:
+            // only the last min(S, issued) slots can be outstanding.
+            const int first = issued > S ? issued - S : 0;
+            for (int j = first; j < issued; ++j)
+                wait_bar(full(j % S), uint32_t((j / S) & 1), p, abort, 0, j, false);
+        }
+        __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer: one thread drives the tensor core
-            int s = 0;
-            uint32_t ph = 0;
-            int a = 0;
-            uint32_t aph = 0;
-            int it = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                if (!wait_bar(acc_empty(a), aph ^ 1u, p, abort, 1, it)) break;
-                tc_fence_after();
-                const uint32_t d = tmem + uint32_t(a * p.acc_cols);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (p.debug_stall && it == 0) {
-                        // Test hook: a barrier nothing arrives on.
-                        if (!wait_bar(stall, 0, p, abort, 1, it)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    if (!wait_bar(full(s), ph, p, abort, 1, it)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_base = sA + uint32_t(s) * p.a_slot;
-                    const uint32_t b_base = sB + uint32_t(s) * p.b_slot;
-                    for (int kk = 0; kk < p.n_kstep; ++kk) {
-                        const uint64_t bdesc = smem_desc(b_base + uint32_t(kk) * 32u, p);
-                        for (int h = 0; h < p.m_halves; ++h) {
-                            const uint64_t adesc =
-                                smem_desc(a_base + uint32_t(h) * 128u * p.row_bytes + uint32_t(kk) * 32u, p);
-                            mma_f16(d + uint32_t(h * p.bn), adesc, bdesc, p.idesc, (kb | kk) != 0 ? 1u : 0u);
-                        }
-                    }
-                    mma_commit(empty(s));  // slot s may be refilled once these MMAs finish
-                    ++it;
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                mma_commit(acc_full(a));  // accumulator a is complete
-                if (++a == p.acc_stages) {
-                    a = 0;
-                    aph ^= 1u;
-                }
-            }
-            // Every MMA this thread issued must finish before TMEM is freed.
-            mma_commit(drain);
-            wait_bar(drain, 0, p, abort, 1, it, false);
+        // ---------------- MMA issuer: the warp runs the loop, lane 0 drives the tensor core.
+        // The k-steps per slot and the M-halves per tile are compile-time in
+        // the issue loop, so each MMA costs one descriptor add.
+        const MmaCtx c{sA, sB, tmem, bars, S, stall, drain};
+        switch (p.n_kstep * 2 + p.m_halves) {
+        case 1 * 2 + 1: mma_role<1, 1>(p, c, abort, lane); break;
+        case 1 * 2 + 2: mma_role<1, 2>(p, c, abort, lane); break;
+        case 2 * 2 + 1: mma_role<2, 1>(p, c, abort, lane); break;
+        case 2 * 2 + 2: mma_role<2, 2>(p, c, abort, lane); break;
+        case 4 * 2 + 1: mma_role<4, 1>(p, c, abort, lane); break;
+        default: mma_role<4, 2>(p, c, abort, lane); break;
         }
     } else {
         // ---------------- epilogue: 4 warps, warp w reads TMEM lanes 32*(w%4)..+31
@@ -282,10 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
             int mb, nb;
             tile_coords(p, t, mb, nb);
             const int m0 = mb * p.bm, n0 = nb * p.bn;
-            int ok = 1;
-            if (lane == 0) ok = wait_bar(acc_full(a), aph, p, abort, 2, tiles_done) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            if (!warp_wait(acc_full(a), aph, p, abort, 2, tiles_done)) break;
             tc_fence_after();
             for (int h = 0; h < p.m_halves; ++h) {
                 const int row0 = m0 + h * 128 + q * 32;

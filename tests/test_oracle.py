@@ -117,6 +117,8 @@ def test_entries_and_rows_agree_with_full():
     r, s = oracle.gemm_entries(A, B, "f16", rows, cols)
     assert np.array_equal(r, R[rows, cols]) and np.array_equal(s, S[rows, cols])
     assert np.array_equal(oracle.gemm_rows(A, B, "f16", 10, 5), R[10:15])
+    Ad, Bd = oracle.decode(A, "f16"), oracle.decode(B, "f16")
+    assert np.array_equal(oracle.gemm_decoded_rows(Ad, Bd, 3, 30), R[3:33])
 
 
 def test_degenerate_shapes():
