@@ -1,0 +1,237 @@
+"""Sweep of (block_M, block_N, block_K, num_stages) for one workload.
+
+The autotuning procedure of the TileLang tutorial, chapter 11 "Pipeline and
+autotuning", restated for this kernel:
+
+* section 3.7: prune the space before building anything -- drop tiles that do
+  not divide the problem (optional here, since the kernel handles ragged
+  edges) and configs whose num_stages x (A tile + B tile) bound exceeds the
+  per-block shared-memory budget (section 4.5), here the limit queried from
+  the device, never a constant;
+* section 3.5: run every surviving candidate on the same inputs, warm-up then
+  timed repetitions, and check each against a reference (here: sampled
+  entries of the fp64 oracle, to the kernel tolerance);
+* section 3.8: read the config, not the latency: the winner (lowest median
+  time; ties within 1 % go to the smaller shared footprint, then to fewer
+  stages) is written to a per-device cache file, and a switch
+  (TGEMM_AUTOTUNE_DISABLE_CACHE=1) forces a new search;
+* the num_stages experiment of the "01-num-stages-ir-diff" README: latency
+  and shared memory against num_stages for several tile shapes, where
+  latency should plateau while shared memory keeps growing.
+
+Usage (on a GB300):
+    python -m software_pipelined_tiled_02_gb300.sweep --workload gemm_4096_f16_normal --space gb300
+    python -m software_pipelined_tiled_02_gb300.sweep --workload gemm_4096_f16_normal --stage-curve
+"""
+
+from __future__ import annotations
+
+import argparse
+import itertools
+import json
+import os
+import statistics
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import software_pipelined_tiled_02_gb300 as tg  # noqa: E402
+from software_pipelined_tiled_02_gb300 import inputs  # noqa: E402
+
+PAGES_SPACE = dict(block_M=(64, 128, 256), block_N=(64, 128, 256), block_K=(16, 32, 64), num_stages=(1, 2, 3, 4))
+GB300_SPACE = dict(block_M=(128, 256), block_N=(64, 128, 192, 224, 256), block_K=(32, 64),
+                   num_stages=(2, 3, 4, 5, 6, 8))
+
+
+def enumerate_space(space: dict):
+    keys = ("block_M", "block_N", "block_K", "num_stages")
+    return [dict(zip(keys, v)) for v in itertools.product(*(space[k] for k in keys))]
+
+
+def prune(configs, M, N, K, dtype, out_dtype, smem_limit, divisible=True):
+    """Split candidates into legal ones and rejects, before anything runs.
+
+    Returns (legal, rejects) where rejects maps a reason to its configs."""
+    legal, rejects = [], {"not_divisible": [], "smem_budget": [], "no_kernel": [], "other": []}
+    for c in configs:
+        if divisible and (M % c["block_M"] or N % c["block_N"] or K % c["block_K"]):
+            rejects["not_divisible"].append(c)
+            continue
+        rc = tg.tgemm_validate(M, N, K, dtype, out_dtype, c["block_M"], c["block_N"], c["block_K"],
+                               c["num_stages"], smem_limit)
+        if rc == tg.OK:
+            legal.append(c)
+        elif rc == tg.ERR_SMEM_BUDGET:
+            rejects["smem_budget"].append(c)
+        elif rc == tg.ERR_NO_KERNEL:
+            rejects["no_kernel"].append(c)
+        else:
+            rejects["other"].append(c)
+    return legal, rejects
+
+
+def pick_best(rows):
+    """Lowest median time; within 1 % prefer the smaller shared footprint, then fewer stages."""
+    ok = [r for r in rows if r.get("ok")]
+    if not ok:
+        return None
+    fastest = min(r["median_ms"] for r in ok)
+    near = [r for r in ok if r["median_ms"] <= fastest * 1.01]
+    return min(near, key=lambda r: (r["smem_bytes"], r["num_stages"], r["median_ms"]))
+
+
+def cache_path(device_name: str, workload: str) -> str:
+    base = os.environ.get("TGEMM_CACHE_DIR", os.path.join(os.path.expanduser("~"), ".cache", "tgemm"))
+    safe = "".join(ch if ch.isalnum() else "_" for ch in device_name)
+    return os.path.join(base, safe, f"{workload}.best_config.json")
+
+
+def load_cached(device_name: str, workload: str):
+    if os.environ.get("TGEMM_AUTOTUNE_DISABLE_CACHE") == "1":
+        return None
+    try:
+        with open(cache_path(device_name, workload)) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+class Runner:
+    """Times candidates of one workload on the current GPU and checks them."""
+
+    def __init__(self, workload: str, reps: int = 20, warmup: int = 5, check_entries: int = 512):
+        import torch
+
+        self.torch = torch
+        self.w = inputs.WORKLOADS[workload]
+        self.name = workload
+        w = self.w
+        self.M, self.N, self.K = w["M"], w["N"], w["K"]
+        self.A, self.B = inputs.workload_operands(workload)
+        self.dA = inputs.bits_to_torch(self.A, w["dtype"]).cuda()
+        self.dB = inputs.bits_to_torch(self.B, w["dtype"]).cuda()
+        tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[w["out"]]
+        self.C = torch.empty((self.M, self.N), dtype=tdt, device="cuda")
+        self.flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+        self.reps, self.warmup = reps, warmup
+        rng = np.random.default_rng(123)
+        self.rows = rng.integers(0, self.M, check_entries)
+        self.cols = rng.integers(0, self.N, check_entries)
+        import oracle
+
+        self.R, self.S = oracle.gemm_entries(self.A, self.B, w["dtype"], self.rows, self.cols)
+        self.oracle = oracle
+
+    def run(self, c: dict) -> dict:
+        torch = self.torch
+        w = self.w
+        row = dict(c)
+        try:
+            plan = tg.Plan(self.M, self.N, self.K, w["dtype"], w["out"],
+                           (c["block_M"], c["block_N"], c["block_K"]), c["num_stages"])
+        except tg.TgemmError as e:
+            row.update(ok=False, error=str(e))
+            return row
+        info = plan.info
+        self.C.fill_(float("nan"))
+        for _ in range(self.warmup):
+            plan.run(self.dA, self.dB, self.C)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(self.reps):
+            self.flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            plan.run(self.dA, self.dB, self.C)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        code, _ = plan.status()
+        got = self.C[torch.from_numpy(self.rows).cuda(), torch.from_numpy(self.cols).cuda()].float().cpu().double()
+        ok, worst, _ = self.oracle.check(got.numpy(), self.R, self.S, w["out"])
+        med = statistics.median(times)
+        row.update(ok=bool(ok and code == tg.OK), worst_error_ratio=worst, median_ms=med, min_ms=min(times),
+                   tflops=2.0 * self.M * self.N * self.K / (med * 1e-3) / 1e12, smem_bytes=info["smem_bytes"],
+                   smem_bound=info["smem_bound"], grid=info["grid"], tiles=info["num_tiles"])
+        plan.close()
+        return row
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description="tile / num_stages sweep")
+    ap.add_argument("--workload", default="gemm_4096_f16_normal")
+    ap.add_argument("--space", choices=("pages", "gb300"), default="gb300")
+    ap.add_argument("--any-tile", action="store_true", help="keep tiles that do not divide the problem")
+    ap.add_argument("--stage-curve", action="store_true", help="latency and smem vs num_stages for 3 tile shapes")
+    ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--out", default=None, help="write all rows as JSON here")
+    ap.add_argument("--no-cache", action="store_true", help="do not write the per-device best config")
+    args = ap.parse_args(argv)
+
+    import torch
+
+    tg.load()
+    w = inputs.WORKLOADS[args.workload]
+    M, N, K = w["M"], w["N"], w["K"]
+    limit = tg.tgemm_smem_limit()
+    dev = torch.cuda.get_device_name()
+    runner = Runner(args.workload, reps=args.reps)
+    report = {"workload": args.workload, "device": dev, "smem_limit": limit}
+
+    if args.stage_curve:
+        curve = []
+        for block in ((128, 128, 32), (128, 256, 64), (256, 256, 64)):
+            for S in (1, 2, 3, 4, 6, 8):
+                c = dict(block_M=block[0], block_N=block[1], block_K=block[2], num_stages=S)
+                rc = tg.tgemm_validate(M, N, K, w["dtype"], w["out"], *block, S, limit)
+                if rc != tg.OK:
+                    curve.append(dict(c, ok=False, rejected=tg.strerror(rc),
+                                      smem_bound=tg.tgemm_smem_bound(w["dtype"], *block, S)))
+                    continue
+                curve.append(runner.run(c))
+        report["stage_curve"] = curve
+        print("| tile | num_stages | median µs | TFLOP/s | smem bound B | smem requested B | parity |")
+        print("|---|---|---|---|---|---|---|")
+        for r in curve:
+            tile = f"{r['block_M']}x{r['block_N']}x{r['block_K']}"
+            if "median_ms" in r:
+                print(f"| {tile} | {r['num_stages']} | {1e3 * r['median_ms']:.1f} | {r['tflops']:.0f} | "
+                      f"{r['smem_bound']} | {r['smem_bytes']} | {'ok' if r['ok'] else 'FAIL'} |")
+            else:
+                print(f"| {tile} | {r['num_stages']} | rejected before launch | - | {r['smem_bound']} | - | - |")
+    else:
+        space = PAGES_SPACE if args.space == "pages" else GB300_SPACE
+        configs = enumerate_space(space)
+        legal, rejects = prune(configs, M, N, K, w["dtype"], w["out"], limit, divisible=not args.any_tile)
+        report["requested"] = len(configs)
+        report["legal"] = len(legal)
+        report["rejected"] = {k: len(v) for k, v in rejects.items()}
+        print(json.dumps({k: report[k] for k in ("workload", "device", "smem_limit", "requested", "legal",
+                                                 "rejected")}), flush=True)
+        rows = [runner.run(c) for c in legal]
+        report["rows"] = rows
+        best = pick_best(rows)
+        report["best"] = best
+        for r in sorted(rows, key=lambda r: r.get("median_ms", 1e9))[:10]:
+            print(json.dumps({k: r[k] for k in ("block_M", "block_N", "block_K", "num_stages", "median_ms",
+                                                "tflops", "smem_bytes", "ok")}), flush=True)
+        if best and not args.no_cache:
+            path = cache_path(dev, args.workload)
+            os.makedirs(os.path.dirname(path), exist_ok=True)
+            with open(path, "w") as f:
+                json.dump(best, f, indent=1)
+        print("best:", json.dumps(best), flush=True)
+        bad = [r for r in rows if not r.get("ok")]
+        if bad:
+            print(f"{len(bad)} candidates failed parity or reported an error", flush=True)
+    if args.out:
+        with open(args.out, "w") as f:
+            json.dump(report, f, indent=1)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,62 @@
+"""Host logic of the sweep: pruning before launch, tie-break, cache switch."""
+
+import oracle
+import software_pipelined_tiled_02_gb300 as tg
+from software_pipelined_tiled_02_gb300 import build as tbuild
+from software_pipelined_tiled_02_gb300 import sweep
+
+LIMIT = 227 * 1024
+
+
+def setup_module(_):
+    tbuild.build()
+    tg.load()
+
+
+def test_pages_space_prunes_over_budget_before_launch():
+    cfgs = sweep.enumerate_space(sweep.PAGES_SPACE)
+    assert len(cfgs) == 3 * 3 * 3 * 4  # the pages' grid without its `threads` axis
+    legal, rej = sweep.prune(cfgs, 4096, 4096, 4096, tg.F16, tg.F16, LIMIT)
+    over = {(c["block_M"], c["block_N"], c["block_K"], c["num_stages"]) for c in rej["smem_budget"]}
+    assert (256, 256, 64, 4) in over
+    # every config the pages' bound puts over the limit is rejected, none is launched
+    for c in cfgs:
+        if c["block_M"] != 64 and oracle.smem_bound(c["block_M"], c["block_N"], c["block_K"],
+                                                    c["num_stages"], 2) > LIMIT:
+            assert c not in legal
+    # block_M = 64 is not implemented by this kernel: reported, not launched
+    assert all(c["block_M"] == 64 for c in rej["no_kernel"]) and rej["no_kernel"]
+    assert not rej["not_divisible"]
+    assert len(legal) + sum(len(v) for v in rej.values()) == len(cfgs)
+
+
+def test_divisibility_prune_is_optional():
+    cfgs = [dict(block_M=128, block_N=192, block_K=64, num_stages=3)]
+    legal, rej = sweep.prune(cfgs, 4096, 4096, 4096, tg.F16, tg.F16, LIMIT, divisible=True)
+    assert not legal and rej["not_divisible"]
+    legal, rej = sweep.prune(cfgs, 4096, 4096, 4096, tg.F16, tg.F16, LIMIT, divisible=False)
+    assert legal == cfgs
+
+
+def test_pick_best_tie_break():
+    rows = [dict(ok=True, median_ms=1.000, smem_bytes=200000, num_stages=4),
+            dict(ok=True, median_ms=1.005, smem_bytes=150000, num_stages=3),
+            dict(ok=True, median_ms=1.005, smem_bytes=150000, num_stages=2),
+            dict(ok=False, median_ms=0.5, smem_bytes=1, num_stages=1),
+            dict(ok=True, median_ms=1.2, smem_bytes=1000, num_stages=1)]
+    best = sweep.pick_best(rows)
+    assert best["smem_bytes"] == 150000 and best["num_stages"] == 2
+    assert sweep.pick_best([dict(ok=False)]) is None
+
+
+def test_cache_switch(tmp_path, monkeypatch):
+    monkeypatch.setenv("TGEMM_CACHE_DIR", str(tmp_path))
+    p = sweep.cache_path("NVIDIA GB300", "wl")
+    import json
+    import os
+
+    os.makedirs(os.path.dirname(p), exist_ok=True)
+    json.dump({"block_M": 256}, open(p, "w"))
+    assert sweep.load_cached("NVIDIA GB300", "wl") == {"block_M": 256}
+    monkeypatch.setenv("TGEMM_AUTOTUNE_DISABLE_CACHE", "1")
+    assert sweep.load_cached("NVIDIA GB300", "wl") is None
