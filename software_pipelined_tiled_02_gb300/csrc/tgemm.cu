@@ -492,6 +492,23 @@ struct tgemm_plan_s {
 
 static const unsigned long long kDefaultWatchdogNs = 2000000000ull;
 
+// The kernel's dynamic shared-memory ceiling is a per-function, per-device
+// attribute: set it once per device to the device's opt-in limit, so that
+// every plan (whatever its own footprint) can launch.
+static int allow_max_smem(int dev, int limit)
+{
+    static std::mutex mu;
+    static bool done[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && done[dev]) return kOk;
+    if (cudaFuncSetAttribute(tgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess) {
+        cudaGetLastError();
+        return kErrCuda;
+    }
+    if (dev >= 0 && dev < 64) done[dev] = true;
+    return kOk;
+}
+
 static unsigned long long env_watchdog()
 {
     const char *e = std::getenv("TGEMM_WATCHDOG_NS");
@@ -594,9 +611,7 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
         delete p;
         return kErrCuda;
     }
-    if (cudaFuncSetAttribute(tgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_launch) !=
-        cudaSuccess) {
-        cudaGetLastError();
+    if (allow_max_smem(dev, limit) != kOk) {
         cudaFree(p->d_status);
         delete p;
         return kErrCuda;

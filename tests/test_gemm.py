@@ -138,6 +138,22 @@ def test_output_not_written_outside_c(cuda_lib):
     assert_close(as_f64(C), R, S, "f32")
 
 
+def test_plans_of_different_footprints_coexist(cuda_lib):
+    # A plan created after a larger one must not shrink what the larger one may launch with.
+    M, N, K = 256, 256, 256
+    A, B = inputs.operands(8, M, N, K, "f16", "uniform")
+    dA, dB = to_dev(A, "f16"), to_dev(B, "f16")
+    big = cuda_lib.Plan(M, N, K, "f16", "f32", (256, 256, 64), 3)
+    small = cuda_lib.Plan(M, N, K, "f16", "f32", (128, 64, 16), 1)
+    assert big.info["smem_bytes"] > small.info["smem_bytes"]
+    R, S = oracle.gemm(A, B, "f16")
+    for plan in (big, small, big):
+        C = plan.run(dA, dB)
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+        assert_close(as_f64(C), R, S, "f32")
+
+
 def test_plan_rejects_over_budget_on_device(cuda_lib):
     rc, h = cuda_lib.tgemm_plan(4000, 3000, 5000, "f16", "f32", 256, 256, 64, 4)
     assert rc == cuda_lib.ERR_SMEM_BUDGET and h is None
