@@ -183,6 +183,38 @@ typedef struct tgemm_plan_info {
 
 int tgemm_get_plan_info(tgemm_plan_t plan, tgemm_plan_info *info);
 
+/*
+ * Allocation-free form of tgemm_plan + tgemm_run (+ tgemm_status), for callers
+ * that cannot allocate device memory: code running where cudaMalloc is
+ * unavailable or must not be called (a custom allocator's own hooks, a service
+ * that fixes its device footprint at start-up, a runtime that hands the library
+ * only the buffers it works on).  The tutorial pages have no counterpart; this
+ * is an interface addition of this library.
+ *
+ * Arguments and checks are those of tgemm_plan and tgemm_run (same status
+ * codes; sizes, dtypes, tiles and depths they reject are rejected here).  The
+ * kernel's only memory besides A, B and C is its 16-byte status record; here it
+ * lives in a fixed 256-byte array inside the library's CUDA module, which every
+ * GPU that loads the library holds until the process exits.  A call that would
+ * need more scratch than that array holds is rejected with
+ * TGEMM_ERR_INVALID_ARG.  The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * The call enqueues on `stream` a clear of the array's status record and the
+ * kernel.  If `status` is non-NULL it then copies the record back, waits for
+ * `stream`, and stores TGEMM_OK or TGEMM_ERR_TIMEOUT there; if NULL the call
+ * returns right after enqueueing.  All calls on a device share the one array:
+ * calls whose kernels overlap on the same GPU (for instance on two streams)
+ * race on it, and the status they report is then unreliable.
+ *
+ * The first call on each device looks up the array's device address and sets
+ * the kernel's shared-memory ceiling for that device; make that first call
+ * before any stream capture.
+ */
+int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N,
+                      int block_K, int num_stages, const void *A, const void *B, void *C, tgemm_stream_t stream,
+                      int *status);
+
 /* Free a plan and its status word.  NULL is accepted (no-op). */
 int tgemm_destroy(tgemm_plan_t plan);
 

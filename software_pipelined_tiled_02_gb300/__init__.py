@@ -27,7 +27,7 @@ _DT_NAMES = {"f16": F16, "bf16": BF16, "f32": F32}
 
 SYMBOLS = ("tgemm_smem_bound", "tgemm_smem_bytes", "tgemm_smem_limit", "tgemm_validate", "tgemm_plan",
            "tgemm_run", "tgemm_run_host", "tgemm_status", "tgemm_set_watchdog_ns", "tgemm_debug_stall",
-           "tgemm_get_plan_info", "tgemm_destroy", "tgemm_strerror")
+           "tgemm_get_plan_info", "tgemm_destroy", "tgemm_strerror", "tgemm_run_noalloc")
 
 
 class TgemmError(RuntimeError):
@@ -88,6 +88,9 @@ def load(path: str = LIB_PATH):
         L.tgemm_get_plan_info.restype = i32
         L.tgemm_destroy.argtypes = [vp]
         L.tgemm_destroy.restype = i32
+        L.tgemm_run_noalloc.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                        ctypes.POINTER(ctypes.c_int)]
+        L.tgemm_run_noalloc.restype = i32
         L.tgemm_strerror.argtypes = [i32]
         L.tgemm_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -169,6 +172,15 @@ def tgemm_get_plan_info(plan) -> dict:
 
 def tgemm_destroy(plan) -> int:
     return int(load().tgemm_destroy(plan))
+
+
+def tgemm_run_noalloc(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, A_ptr: int, B_ptr: int,
+                      C_ptr: int, stream: int = 0, want_status: bool = True):
+    """The allocation-free entry point: returns (return code, kernel status or None)."""
+    st = ctypes.c_int(-1)
+    rc = load().tgemm_run_noalloc(M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K, num_stages,
+                                  A_ptr, B_ptr, C_ptr, stream, ctypes.byref(st) if want_status else None)
+    return int(rc), (int(st.value) if want_status else None)
 
 
 def strerror(code: int) -> str:

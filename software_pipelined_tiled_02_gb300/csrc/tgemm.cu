@@ -820,3 +820,148 @@ const char *tgemm_strerror(int code)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free entry point
+//
+// For callers that cannot allocate device memory: code that runs where
+// cudaMalloc is unavailable or must not be called (inside a custom allocator's
+// own hooks, in a service that fixes its device footprint at start-up, or in a
+// host runtime that hands the library only the buffers it works on).
+// tgemm_plan allocates the kernel's status record with cudaMalloc, so such
+// callers cannot use it.  tgemm_run_noalloc runs the same kernel with that
+// record -- the only global memory the kernel touches besides A, B and C --
+// in the file-scope array below, which the CUDA module provides: every GPU
+// that loads this library holds these 256 bytes until the process exits.
+
+static constexpr int kNoallocScratchInts = 64;  // 256 bytes; the kernel needs one 4-int record
+static __device__ __align__(256) int g_noalloc_scratch[kNoallocScratchInts];
+
+// Once per device, with that device current: the array's device address
+// (host code only sees a host-side stand-in for the symbol) and the kernel's
+// shared-memory ceiling.
+static int noalloc_setup(int dev, int limit, int **scratch)
+{
+    static std::mutex mu;
+    static int *addr[64] = {};
+    if (dev < 0 || dev >= 64) return kErrInvalidArg;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return kErrCuda;
+        }
+        addr[dev] = static_cast<int *>(p);
+    }
+    if (allow_max_smem(dev, limit) != kOk) return kErrCuda;
+    *scratch = addr[dev];
+    return kOk;
+}
+
+extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N,
+                                 int block_K, int num_stages, const void *A, const void *B, void *C,
+                                 tgemm_stream_t stream, int *status)
+{
+    const size_t need_bytes = 4 * sizeof(int);  // the status record
+    if (need_bytes > sizeof(g_noalloc_scratch)) return kErrInvalidArg;
+    int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX);
+    if (rc != kOk) return rc;
+    int dev = 0, major = 0, minor = 0, sms = 0, limit = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ||
+        cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ||
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) {
+        cudaGetLastError();
+        return kErrCuda;
+    }
+    if (major != 10 || minor != 3) return kErrArch;
+    rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit);
+    if (rc != kOk) return rc;
+    if (status) *status = kOk;
+    if (M == 0 || N == 0) return kOk;  // empty product: nothing to write
+    if (!C || (K > 0 && (!A || !B))) return kErrInvalidArg;
+    if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return kErrAlignment;
+    int *scratch = nullptr;
+    rc = noalloc_setup(dev, limit, &scratch);
+    if (rc != kOk) return rc;
+
+    const Layout L = make_layout(block_M, block_N, block_K, num_stages, dtype, out_dtype);
+    const int one_per_sm = per_sm / 2 + 1;
+    int smem = int(L.total) > one_per_sm ? int(L.total) : one_per_sm;
+    if (smem > limit) smem = limit;
+    const int tiles_m = int((M + block_M - 1) / block_M);
+    const int tiles_n = int((N + block_N - 1) / block_N);
+    const int tiles = tiles_m * tiles_n;
+    const int grid = tiles < sms ? tiles : sms;
+
+    Params q;
+    std::memset(&q, 0, sizeof(q));
+    q.M = int(M);
+    q.N = int(N);
+    q.K = int(K);
+    q.num_kb = int((K + block_K - 1) / block_K);
+    q.tiles_m = tiles_m;
+    q.tiles_n = tiles_n;
+    q.num_tiles = tiles;
+    q.group_m = 8;
+    q.bm = block_M;
+    q.bn = block_N;
+    q.bk = block_K;
+    q.stages = num_stages;
+    q.n_kstep = block_K * L.in_bytes / 32;
+    q.m_halves = L.m_halves;
+    q.out_mode = out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
+    q.acc_stages = L.acc_stages;
+    q.acc_cols = L.acc_cols;
+    q.tmem_cols = L.tmem_cols;
+    const uint32_t ab = dtype == kBF16 ? 1u : 0u;
+    q.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(block_N >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    q.a_slot = round_up(L.a_stage_bytes, kSmemAlign);
+    q.b_slot = round_up(L.b_stage_bytes, kSmemAlign);
+    q.stage_tx = L.a_stage_bytes + L.b_stage_bytes;
+    q.row_bytes = uint32_t(L.swizzle_bytes);
+    q.off_a = L.off_a;
+    q.off_b = L.off_b;
+    q.off_c = L.off_c;
+    q.off_bar = L.off_bar;
+    q.c_buf_bytes = L.c_buf_bytes;
+    q.desc_lo_flags = (1u << 16);
+    const uint32_t sbo = 8u * uint32_t(L.swizzle_bytes);
+    q.desc_hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (desc_layout_for(L.swizzle_bytes) << 29);
+    q.watchdog_ns = env_watchdog();
+    q.status = scratch;
+    q.debug_stall = 0;
+    if (K > 0) {
+        const CUtensorMapSwizzle swz = swizzle_for(L.swizzle_bytes);
+        rc = encode_2d(&q.tmA, dtype, A, uint64_t(K), uint64_t(M), uint64_t(K) * L.in_bytes, uint32_t(L.bk),
+                       uint32_t(L.bm), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        if (rc == kOk)
+            rc = encode_2d(&q.tmB, dtype, B, uint64_t(K), uint64_t(N), uint64_t(K) * L.in_bytes, uint32_t(L.bk),
+                           uint32_t(L.bn), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    }
+    if (rc == kOk)
+        rc = encode_2d(&q.tmC, out_dtype, C, uint64_t(N), uint64_t(M), uint64_t(N) * L.out_bytes,
+                       uint32_t(kEpiCols), 32u, L.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                       CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (rc != kOk) return rc;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's record: clear it before this launch.
+    if (cudaMemsetAsync(scratch, 0, need_bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return kErrCuda;
+    }
+    tgemm_kernel<<<grid, kThreads, smem, s>>>(q);
+    if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+    if (status) {
+        int h[4] = {0, 0, 0, 0};
+        if (cudaMemcpyAsync(h, scratch, need_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess) {
+            cudaGetLastError();
+            return kErrCuda;
+        }
+        *status = h[0];
+    }
+    return kOk;
+}
