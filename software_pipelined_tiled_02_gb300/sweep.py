@@ -203,6 +203,19 @@ def main(argv=None):
                       f"{r['smem_bound']} | {r['smem_bytes']} | {'ok' if r['ok'] else 'FAIL'} |")
             else:
                 print(f"| {tile} | {r['num_stages']} | rejected before launch | - | {r['smem_bound']} | - | - |")
+        # Fit the pipeline model of chapter 11 section 1.3 to each tile's curve.
+        from software_pipelined_tiled_02_gb300 import pipeline_model
+
+        fits = {}
+        for block in sorted({(r["block_M"], r["block_N"], r["block_K"]) for r in curve}):
+            pts = {r["num_stages"]: r["median_ms"] for r in curve
+                   if (r["block_M"], r["block_N"], r["block_K"]) == block and "median_ms" in r}
+            if len(pts) >= 2:
+                f = pipeline_model.fit(pts)
+                fits["x".join(map(str, block))] = {k: f[k] for k in ("ratio", "min_depth", "rms")}
+                print(f"model fit {block}: latency/compute = {f['ratio']:.2f}, "
+                      f"model's sufficient depth = {f['min_depth']}")
+        report["model_fit"] = fits
     else:
         space = PAGES_SPACE if args.space == "pages" else GB300_SPACE
         configs = enumerate_space(space)
