@@ -121,6 +121,32 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
                int block_M, int block_N, int block_K, int num_stages);
 
 /*
+ * Options of tgemm_plan_ex (zero-initialise, then set what you need).
+ *   cta_pair: 0 = one CTA per output tile (tgemm_plan's behaviour).  1 = pairs
+ *     of CTAs (thread-block clusters of 2) on neighbouring SMs share each
+ *     block_M = 256 tile: one M = 256 tensor-core instruction per K step spans
+ *     both SMs, each CTA holds 128 rows of A, block_N / 2 rows of B and 128
+ *     rows of the accumulator.  Only block_M = 256 is accepted.  Each CTA is a
+ *     block in the sense of the pages' budget rule: the bound checked is
+ *     num_stages x (128 x block_K + block_K x block_N / 2) x element size.
+ *   group_m: M-tiles per raster group of the persistent schedule (0: 8).
+ */
+typedef struct tgemm_plan_opts {
+    int cta_pair;
+    int group_m;
+} tgemm_plan_opts;
+
+/* tgemm_validate with options (NULL = defaults). */
+int tgemm_validate_ex(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M,
+                      int block_N, int block_K, int num_stages, int64_t smem_limit,
+                      const tgemm_plan_opts *opts);
+
+/* tgemm_plan with options (NULL = defaults); ERR_INVALID_ARG for an option out
+ * of range, ERR_NO_KERNEL for cta_pair with block_M != 256. */
+int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
+                  int block_M, int block_N, int block_K, int num_stages, const tgemm_plan_opts *opts);
+
+/*
  * Enqueue C = A . B^T on `stream`.  A, B, C are device pointers with the
  * layouts above (16-byte aligned, caller-owned; C must not overlap A or B).
  * Returns after the launch is enqueued; results are ready when the stream
@@ -179,6 +205,7 @@ typedef struct tgemm_plan_info {
     int64_t smem_bound;  /* the pages' num_stages * (A + B tile) bound */
     int smem_limit;      /* device per-block limit at plan time */
     int num_sms;
+    int cta_pair;        /* 1: clusters of two CTAs share each tile */
 } tgemm_plan_info;
 
 int tgemm_get_plan_info(tgemm_plan_t plan, tgemm_plan_info *info);

@@ -27,7 +27,8 @@ _DT_NAMES = {"f16": F16, "bf16": BF16, "f32": F32}
 
 SYMBOLS = ("tgemm_smem_bound", "tgemm_smem_bytes", "tgemm_smem_limit", "tgemm_validate", "tgemm_plan",
            "tgemm_run", "tgemm_run_host", "tgemm_status", "tgemm_set_watchdog_ns", "tgemm_debug_stall",
-           "tgemm_get_plan_info", "tgemm_destroy", "tgemm_strerror", "tgemm_run_noalloc")
+           "tgemm_get_plan_info", "tgemm_destroy", "tgemm_strerror", "tgemm_run_noalloc", "tgemm_plan_ex",
+           "tgemm_validate_ex")
 
 
 class TgemmError(RuntimeError):
@@ -43,10 +44,15 @@ class PlanInfo(ctypes.Structure):
                 ("tiles_m", ctypes.c_int), ("tiles_n", ctypes.c_int), ("num_tiles", ctypes.c_int),
                 ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("num_k_blocks", ctypes.c_int),
                 ("acc_stages", ctypes.c_int), ("tmem_columns", ctypes.c_int), ("smem_bytes", ctypes.c_int64),
-                ("smem_bound", ctypes.c_int64), ("smem_limit", ctypes.c_int), ("num_sms", ctypes.c_int)]
+                ("smem_bound", ctypes.c_int64), ("smem_limit", ctypes.c_int), ("num_sms", ctypes.c_int),
+                ("cta_pair", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class PlanOpts(ctypes.Structure):
+    _fields_ = [("cta_pair", ctypes.c_int), ("group_m", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -91,6 +97,11 @@ def load(path: str = LIB_PATH):
         L.tgemm_run_noalloc.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                         ctypes.POINTER(ctypes.c_int)]
         L.tgemm_run_noalloc.restype = i32
+        L.tgemm_plan_ex.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i32, i32, i32, i32, i32, i32,
+                                    ctypes.POINTER(PlanOpts)]
+        L.tgemm_plan_ex.restype = i32
+        L.tgemm_validate_ex.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, i64, ctypes.POINTER(PlanOpts)]
+        L.tgemm_validate_ex.restype = i32
         L.tgemm_strerror.argtypes = [i32]
         L.tgemm_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -138,6 +149,22 @@ def tgemm_plan(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages)
     rc = load().tgemm_plan(ctypes.byref(h), M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K,
                            num_stages)
     return int(rc), (h if rc == OK else None)
+
+
+def tgemm_plan_ex(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, cta_pair=0, group_m=0):
+    """Returns ``(status, handle)``; handle is None on failure."""
+    h = ctypes.c_void_p()
+    opts = PlanOpts(int(cta_pair), int(group_m))
+    rc = load().tgemm_plan_ex(ctypes.byref(h), M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K,
+                              num_stages, ctypes.byref(opts))
+    return int(rc), (h if rc == OK else None)
+
+
+def tgemm_validate_ex(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit, cta_pair=0,
+                      group_m=0) -> int:
+    opts = PlanOpts(int(cta_pair), int(group_m))
+    return int(load().tgemm_validate_ex(M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K,
+                                        num_stages, smem_limit, ctypes.byref(opts)))
 
 
 def tgemm_run(plan, A_ptr: int, B_ptr: int, C_ptr: int, stream: int = 0) -> int:
@@ -198,13 +225,18 @@ tgemm_strerror = strerror
 class Plan:
     """A validated GEMM configuration on the current CUDA device."""
 
-    def __init__(self, M, N, K, dtype="f16", out_dtype=None, block=(128, 256, 64), num_stages=4):
+    def __init__(self, M, N, K, dtype="f16", out_dtype=None, block=(128, 256, 64), num_stages=4, pair=False):
         dtype = _dt(dtype)
         out_dtype = dtype if out_dtype is None else _dt(out_dtype)
         bm, bn, bk = block
-        rc, h = tgemm_plan(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages)
+        if pair:
+            rc, h = tgemm_plan_ex(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages, cta_pair=1)
+        else:
+            rc, h = tgemm_plan(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages)
         if rc != OK:
-            raise TgemmError(rc, f"tgemm_plan(M={M}, N={N}, K={K}, block={block}, num_stages={num_stages})")
+            raise TgemmError(rc, f"tgemm_plan(M={M}, N={N}, K={K}, block={block}, num_stages={num_stages}, "
+                                 f"pair={pair})")
+        self.pair = bool(pair)
         self.handle = h
         self.M, self.N, self.K = M, N, K
         self.dtype, self.out_dtype = dtype, out_dtype
@@ -280,13 +312,13 @@ _plans: dict = {}
 
 
 def default_config(M, N, K, dtype="f16", out_dtype=None):
-    """The tuned default (block, num_stages) for a shape."""
+    """The tuned default (block, num_stages, cta_pair) for a shape."""
     from . import defaults
 
     return defaults.choose(M, N, K, _dt(dtype), _dt(dtype) if out_dtype is None else _dt(out_dtype))
 
 
-def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=None):
+def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=None, pair=None):
     """``A[M,K] . B[N,K]^T`` on the GPU through ``libtgemm.so``.
 
     ``out_dtype`` defaults to the operand dtype; ``torch.float32`` returns the
@@ -299,11 +331,13 @@ def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=Non
     dt = _dt(A.dtype)
     odt = dt if out_dtype is None else _dt(out_dtype)
     if block is None or num_stages is None:
-        b, s = default_config(M, N, K, dt, odt)
+        b, s, pr = default_config(M, N, K, dt, odt)
         block = block or b
         num_stages = num_stages or s
-    key = (M, N, K, dt, odt, tuple(block), num_stages, A.device.index)
+        pair = pr if pair is None else pair
+    pair = bool(pair)
+    key = (M, N, K, dt, odt, tuple(block), num_stages, pair, A.device.index)
     plan = _plans.get(key)
     if plan is None:
-        plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages)
+        plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages, pair=pair)
     return plan.run(A, B, out, stream)

@@ -33,6 +33,8 @@ inline int dtype_bytes(int dt) { return dt == kF32 ? 4 : (dt == kF16 || dt == kB
 
 struct Layout {
     int bm, bn, bk, stages;
+    int pair;                // 1: two CTAs (a cluster of 2) share one block_M = 256 tile
+    int a_rows, b_rows;      // operand rows one CTA holds per slot (pair: 128 and block_N / 2)
     int in_bytes, out_bytes;
     uint32_t a_stage_bytes;  // bm * bk * in_bytes
     uint32_t b_stage_bytes;  // bn * bk * in_bytes
@@ -53,8 +55,11 @@ inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 // Tile shapes the kernel implements: M = 128 MMAs (one or two per k-step),
 // N a multiple of 32 up to the MMA maximum of 256, and block_K such that a
 // K-contiguous operand row is exactly one swizzle span (32, 64 or 128 bytes).
-inline bool tile_supported(int bm, int bn, int bk, int in_bytes)
+// The CTA-pair mode implements only block_M = 256 (one M = 256 MMA over the
+// two CTAs' 128-row halves).
+inline bool tile_supported(int bm, int bn, int bk, int in_bytes, int pair = 0)
 {
+    if (pair && bm != 256) return false;
     if (bm != 128 && bm != 256) return false;
     if (bn < 32 || bn > 256 || bn % 32 != 0) return false;
     int row = bk * in_bytes;
@@ -65,18 +70,22 @@ inline bool tile_supported(int bm, int bn, int bk, int in_bytes)
 // (8 bytes each), then the TMEM base address word and the abort flag.
 inline uint32_t barrier_block_bytes(int stages) { return round_up((2u * stages + 6u) * 8u + 8u, 16u); }
 
-inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out_dtype)
+inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out_dtype, int pair = 0)
 {
     Layout L{};
     L.bm = bm;
     L.bn = bn;
     L.bk = bk;
     L.stages = stages;
+    L.pair = pair ? 1 : 0;
+    L.a_rows = pair ? bm / 2 : bm;
+    L.b_rows = pair ? bn / 2 : bn;
     L.in_bytes = dtype_bytes(dtype);
     L.out_bytes = dtype_bytes(out_dtype);
-    L.a_stage_bytes = uint32_t(bm) * bk * L.in_bytes;
-    L.b_stage_bytes = uint32_t(bn) * bk * L.in_bytes;
-    L.bound = int64_t(stages) * (int64_t(bm) * bk + int64_t(bk) * bn) * L.in_bytes;
+    L.a_stage_bytes = uint32_t(L.a_rows) * bk * L.in_bytes;
+    L.b_stage_bytes = uint32_t(L.b_rows) * bk * L.in_bytes;
+    // The pages' bound for the operand tiles one CTA (one block) holds.
+    L.bound = int64_t(stages) * (int64_t(L.a_rows) * bk + int64_t(bk) * L.b_rows) * L.in_bytes;
     L.c_buf_bytes = 32u * kEpiCols * L.out_bytes;
     L.off_a = 0;
     L.off_b = L.off_a + uint32_t(stages) * round_up(L.a_stage_bytes, kSmemAlign);
@@ -84,7 +93,7 @@ inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out
     L.off_bar = L.off_c + round_up(uint32_t(kEpiWarps * kEpiBufs) * L.c_buf_bytes, kSmemAlign);
     L.bar_bytes = barrier_block_bytes(stages);
     L.total = L.off_bar + L.bar_bytes + kSmemAlign;  // slack to align the dynamic base
-    L.m_halves = bm / 128;
+    L.m_halves = pair ? 1 : bm / 128;
     L.acc_cols = L.m_halves * bn;
     L.acc_stages = (2 * L.acc_cols <= kTmemColsMax) ? 2 : 1;
     int need = L.acc_stages * L.acc_cols;
@@ -97,7 +106,7 @@ inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out
 
 // Every check of tgemm_validate, in the documented order.
 inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int bm, int bn, int bk,
-                    int stages, int64_t smem_limit)
+                    int stages, int64_t smem_limit, int pair = 0)
 {
     if (dtype != kF16 && dtype != kBF16) return kErrUnsupportedDtype;
     if (out_dtype != kF32 && out_dtype != dtype) return kErrUnsupportedDtype;
@@ -106,9 +115,9 @@ inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, i
     if (stages < 1) return kErrInvalidArg;
     if ((K * dtype_bytes(dtype)) % 16 != 0) return kErrAlignment;
     if ((N * dtype_bytes(out_dtype)) % 16 != 0) return kErrAlignment;
-    if (!tile_supported(bm, bn, bk, dtype_bytes(dtype))) return kErrNoKernel;
+    if (!tile_supported(bm, bn, bk, dtype_bytes(dtype), pair)) return kErrNoKernel;
     if (stages > 64) return kErrSmemBudget;  // keeps the layout arithmetic in 32 bits
-    Layout L = make_layout(bm, bn, bk, stages, dtype, out_dtype);
+    Layout L = make_layout(bm, bn, bk, stages, dtype, out_dtype, pair);
     if (L.bound > smem_limit || int64_t(L.total) > smem_limit) return kErrSmemBudget;
     return kOk;
 }

@@ -61,7 +61,8 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     int tiles_m, tiles_n, num_tiles, group_m;
     int bm, bn, bk, stages;
     int n_kstep;                // bk / 16 MMAs along K per slot
-    int m_halves;               // bm / 128
+    int m_halves;               // bm / 128 (1 in pair mode: one M = 256 MMA covers both CTAs)
+    int a_rows, b_rows;         // operand rows this CTA loads per slot (pair: 128 and bn / 2)
     int out_mode;               // 0 fp32, 1 fp16, 2 bf16
     int acc_stages, acc_cols, tmem_cols;
     uint32_t idesc;             // tcgen05 instruction descriptor (kind::f16)
@@ -146,13 +147,16 @@ struct MmaCtx {
     uint32_t sA, sB, tmem, bars;
     int S;
     uint32_t stall, drain;
+    int unit0, ustride;  // first tile and tile stride of this CTA (or CTA pair)
 };
 
 // The MMA warp's main loop.  NK = MMAs of K = 16 per ring slot (block_K / 16),
-// MH = MMAs of M = 128 per k-step (block_M / 128).  Descriptors of slot s are
-// the slot-0 descriptors plus s slot strides (address field in 16-byte units);
-// k-step kk adds 32 bytes, the second M-half adds 128 operand rows.
-template <int NK, int MH>
+// MH = MMAs of M = 128 per k-step (block_M / 128; 1 in pair mode, where one
+// M = 256 MMA spans both CTAs).  Descriptors of slot s are the slot-0
+// descriptors plus s slot strides (address field in 16-byte units); k-step kk
+// adds 32 bytes, the second M-half adds 128 operand rows.  In pair mode this
+// runs in the even CTA only: its commits arrive on the barriers of both CTAs.
+template <int NK, int MH, bool PAIR>
 __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volatile int *abort, int lane)
 {
     const int S = c.S;
@@ -160,10 +164,21 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
     auto empty = [&](int s) { return c.bars + 8u * uint32_t(S + s); };
     auto acc_full = [&](int a) { return c.bars + 8u * uint32_t(2 * S + a); };
     auto acc_empty = [&](int a) { return c.bars + 8u * uint32_t(2 * S + 2 + a); };
+    auto mma = [&](uint32_t d, uint64_t ad, uint64_t bd, uint32_t acc) {
+        if constexpr (PAIR)
+            mma_f16_pair(d, ad, bd, p.idesc, acc);
+        else
+            mma_f16(d, ad, bd, p.idesc, acc);
+    };
+    auto commit_both = [&](uint32_t bar) {
+        if constexpr (PAIR)
+            mma_commit_pair(bar, uint16_t(0x3));
+        else
+            mma_commit(bar);
+    };
     const uint64_t ad0 = smem_desc(c.sA, p), bd0 = smem_desc(c.sB, p);
     const uint64_t a_step = p.a_slot >> 4, b_step = p.b_slot >> 4;
     const uint64_t a_half = (128u * p.row_bytes) >> 4;
-    const uint32_t idesc = p.idesc;
     int s = 0;
     uint32_t ph = 0;
     uint64_t ad = ad0, bd = bd0;
@@ -172,7 +187,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
     int it = 0;
     bool ok = true;
     if (p.debug_stall) ok = warp_wait(c.stall, 0, p, abort, 1, 0);  // test hook: nothing arrives
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+    for (int t = c.unit0; ok && t < p.num_tiles; t += c.ustride) {
         if (!warp_wait(acc_empty(a), aph ^ 1u, p, abort, 1, it)) break;
         tc_fence_after();
         const uint32_t d = c.tmem + uint32_t(a * p.acc_cols);
@@ -189,10 +204,10 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
                 for (int kk = 0; kk < NK; ++kk) {
 #pragma unroll
                     for (int h = 0; h < MH; ++h)
-                        mma_f16(h ? d2 : d, ad + uint64_t(2 * kk) + (h ? a_half : 0), bd + uint64_t(2 * kk), idesc,
-                                kk == 0 ? first : 1u);
+                        mma(h ? d2 : d, ad + uint64_t(2 * kk) + (h ? a_half : 0), bd + uint64_t(2 * kk),
+                            kk == 0 ? first : 1u);
                 }
-                mma_commit(empty(s));  // slot s may be refilled once these MMAs finish
+                commit_both(empty(s));  // slot s (in both CTAs) may be refilled once these MMAs finish
             }
             __syncwarp();
             ++it;
@@ -207,7 +222,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
             }
         }
         if (!ok) break;
-        if (lane == 0) mma_commit(acc_full(a));  // accumulator a is complete
+        if (lane == 0) commit_both(acc_full(a));  // accumulator a is complete (in both CTAs)
         __syncwarp();
         if (++a == p.acc_stages) {
             a = 0;
@@ -216,12 +231,33 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
     }
     // Every MMA this warp issued must finish before TMEM is freed.
     if (lane == 0) {
-        mma_commit(c.drain);
+        if constexpr (PAIR)
+            mma_commit_pair(c.drain, uint16_t(0x1));
+        else
+            mma_commit(c.drain);
         wait_bar(c.drain, 0, p, abort, 1, it, false);
     }
     __syncwarp();
 }
 
+template <int MH, bool PAIR>
+__device__ __forceinline__ void mma_dispatch_nk(const Params &p, const MmaCtx &c, volatile int *abort, int lane)
+{
+    switch (p.n_kstep) {
+    case 1: mma_role<1, MH, PAIR>(p, c, abort, lane); break;
+    case 2: mma_role<2, MH, PAIR>(p, c, abort, lane); break;
+    default: mma_role<4, MH, PAIR>(p, c, abort, lane); break;
+    }
+}
+
+// One kernel, two launch shapes.  PAIR = false: one CTA per tile.  PAIR =
+// true: clusters of two CTAs; the pair computes one block_M = 256 tile with
+// one M = 256 MMA per k-step issued by the even CTA, each CTA holding 128
+// rows of A, half of B's block_N rows and 128 rows of the accumulator.  The
+// pair shares one pipeline: both CTAs' TMA loads complete the even CTA's
+// full[s], and the even CTA's commits arrive on both CTAs' empty[s] and
+// acc_full[a]; both CTAs' epilogues arrive on the even CTA's acc_empty[a].
+template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constant__ Params p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -245,6 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
 
     const int warp = int(threadIdx.x) / 32;
     const int lane = int(threadIdx.x) % 32;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0: the pair's MMA-issuing CTA
+    const int unit0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
+    const int ustride = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -253,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(acc_full(a), 1);
-            mbar_init(acc_empty(a), kEpiWarps);
+            mbar_init(acc_empty(a), PAIR ? 2 * kEpiWarps : kEpiWarps);
         }
         mbar_init(drain, 1);
         mbar_init(stall, 1);
@@ -266,34 +305,51 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         prefetch_tmap(&p.tmC);
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), uint32_t(p.tmem_cols));
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_addr(tmem_slot), uint32_t(p.tmem_cols));
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_addr(tmem_slot), uint32_t(p.tmem_cols));
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
         // ---------------- producer: fill the ring, up to num_stages slots ahead.
         // The whole warp runs the loop (warp-uniform control); lane 0 issues.
+        // Pair mode: each CTA loads its own rows of A and B into its own slot;
+        // both complete the even CTA's full[s], which the even CTA arms with
+        // the bytes of both.
+        const uint32_t full_leader = PAIR ? map_to_rank(full(0), 0) : 0u;
         int s = 0;
         uint32_t ph = 0;
         int issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        for (int t = unit0; ok && t < p.num_tiles; t += ustride) {
             int mb, nb;
             tile_coords(p, t, mb, nb);
-            const int m0 = mb * p.bm, n0 = nb * p.bn;
+            const int m0 = mb * p.bm + int(rank) * p.a_rows, n0 = nb * p.bn + int(rank) * p.b_rows;
             for (int kb = 0; kb < p.num_kb; ++kb) {
                 if (!warp_wait(empty(s), ph ^ 1u, p, abort, 0, issued)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(full(s), p.stage_tx);
-                    tma_load_2d(sA + uint32_t(s) * p.a_slot, &p.tmA, kb * p.bk, m0, full(s));
-                    tma_load_2d(sB + uint32_t(s) * p.b_slot, &p.tmB, kb * p.bk, n0, full(s));
+                    if constexpr (PAIR) {
+                        const uint32_t fb = full_leader + 8u * uint32_t(s);
+                        if (rank == 0) mbar_arrive_expect_tx(full(s), p.stage_tx);
+                        tma_load_2d_pair(sA + uint32_t(s) * p.a_slot, &p.tmA, kb * p.bk, m0, fb);
+                        tma_load_2d_pair(sB + uint32_t(s) * p.b_slot, &p.tmB, kb * p.bk, n0, fb);
+                    } else {
+                        mbar_arrive_expect_tx(full(s), p.stage_tx);
+                        tma_load_2d(sA + uint32_t(s) * p.a_slot, &p.tmA, kb * p.bk, m0, full(s));
+                        tma_load_2d(sB + uint32_t(s) * p.b_slot, &p.tmB, kb * p.bk, n0, full(s));
+                    }
                 }
                 __syncwarp();
                 ++issued;
@@ -306,23 +362,29 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         if (!ok && lane == 0) {
             // Let the loads still in flight land before the CTA may exit:
             // only the last min(S, issued) slots can be outstanding.
-            const int first = issued > S ? issued - S : 0;
-            for (int j = first; j < issued; ++j)
-                wait_bar(full(j % S), uint32_t((j / S) & 1), p, abort, 0, j, false);
+            if (!PAIR || rank == 0) {
+                const int first = issued > S ? issued - S : 0;
+                for (int j = first; j < issued; ++j)
+                    wait_bar(full(j % S), uint32_t((j / S) & 1), p, abort, 0, j, false);
+            } else {
+                // The odd CTA's loads complete the even CTA's barriers, which it
+                // cannot wait on: give them a fixed, generous time to land.
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < 2000000ull) {
+                }
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ---------------- MMA issuer: the warp runs the loop, lane 0 drives the tensor core.
         // The k-steps per slot and the M-halves per tile are compile-time in
         // the issue loop, so each MMA costs one descriptor add.
-        const MmaCtx c{sA, sB, tmem, bars, S, stall, drain};
-        switch (p.n_kstep * 2 + p.m_halves) {
-        case 1 * 2 + 1: mma_role<1, 1>(p, c, abort, lane); break;
-        case 1 * 2 + 2: mma_role<1, 2>(p, c, abort, lane); break;
-        case 2 * 2 + 1: mma_role<2, 1>(p, c, abort, lane); break;
-        case 2 * 2 + 2: mma_role<2, 2>(p, c, abort, lane); break;
-        case 4 * 2 + 1: mma_role<4, 1>(p, c, abort, lane); break;
-        default: mma_role<4, 2>(p, c, abort, lane); break;
+        if (!PAIR || rank == 0) {
+            const MmaCtx c{sA, sB, tmem, bars, S, stall, drain, unit0, ustride};
+            if (p.m_halves == 2)
+                mma_dispatch_nk<2, PAIR>(p, c, abort, lane);
+            else
+                mma_dispatch_nk<1, PAIR>(p, c, abort, lane);
         }
     } else {
         // ---------------- epilogue: 4 warps, warp w reads TMEM lanes 32*(w%4)..+31
@@ -333,10 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         uint32_t aph = 0;
         uint32_t chunk = 0;
         int tiles_done = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tiles_done) {
+        for (int t = unit0; t < p.num_tiles; t += ustride, ++tiles_done) {
             int mb, nb;
             tile_coords(p, t, mb, nb);
-            const int m0 = mb * p.bm, n0 = nb * p.bn;
+            const int m0 = mb * p.bm + int(rank) * p.a_rows, n0 = nb * p.bn;
             if (!warp_wait(acc_full(a), aph, p, abort, 2, tiles_done)) break;
             tc_fence_after();
             for (int h = 0; h < p.m_halves; ++h) {
@@ -396,7 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
             // All TMEM reads of accumulator a are done: hand it back to the MMA warp.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty(a));
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_cluster(map_to_rank(acc_empty(a), 0));
+                else
+                    mbar_arrive(acc_empty(a));
+            }
             if (++a == p.acc_stages) {
                 a = 0;
                 aph ^= 1u;
@@ -408,10 +475,14 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // neither CTA leaves while the pair's MMAs or arrivals may touch it
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        tmem_dealloc(tmem, uint32_t(p.tmem_cols));
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem, uint32_t(p.tmem_cols));
+        else
+            tmem_dealloc(tmem, uint32_t(p.tmem_cols));
     }
 }
 
@@ -480,6 +551,7 @@ struct tgemm_plan_s {
     int smem_limit;
     int smem_launch;
     int tiles_m, tiles_n, num_tiles, grid, group_m;
+    int pair;  // clusters of two CTAs per block_M = 256 tile
     int *d_status;
     unsigned long long watchdog_ns;
     int debug_stall;
@@ -501,7 +573,9 @@ static int allow_max_smem(int dev, int limit)
     static bool done[64] = {};
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && done[dev]) return kOk;
-    if (cudaFuncSetAttribute(tgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess) {
+    if (cudaFuncSetAttribute(tgemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(tgemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess) {
         cudaGetLastError();
         return kErrCuda;
     }
@@ -558,13 +632,29 @@ int tgemm_validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, in
     return validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit);
 }
 
+int tgemm_validate_ex(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N,
+                      int block_K, int num_stages, int64_t smem_limit, const tgemm_plan_opts *opts)
+{
+    return validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit,
+                    opts ? opts->cta_pair : 0);
+}
+
 int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N,
                int block_K, int num_stages)
 {
+    return tgemm_plan_ex(out, M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, nullptr);
+}
+
+int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M,
+                  int block_N, int block_K, int num_stages, const tgemm_plan_opts *opts)
+{
     if (!out) return kErrInvalidArg;
     *out = nullptr;
+    const int pair = opts && opts->cta_pair ? 1 : 0;
+    if (opts && (opts->cta_pair != 0 && opts->cta_pair != 1)) return kErrInvalidArg;
+    if (opts && (opts->group_m < 0 || opts->group_m > 4096)) return kErrInvalidArg;
     // Argument checks that need no device come first.
-    int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX);
+    int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX, pair);
     if (rc != kOk) return rc;
     int dev = 0, major = 0, minor = 0, sms = 0, limit = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
@@ -576,7 +666,7 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
         return kErrCuda;
     }
     if (major != 10 || minor != 3) return kErrArch;
-    rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit);
+    rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit, pair);
     if (rc != kOk) return rc;
 
     tgemm_plan_s *p = new (std::nothrow) tgemm_plan_s();
@@ -586,7 +676,8 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
     p->K = K;
     p->dtype = dtype;
     p->out_dtype = out_dtype;
-    p->L = make_layout(block_M, block_N, block_K, num_stages, dtype, out_dtype);
+    p->L = make_layout(block_M, block_N, block_K, num_stages, dtype, out_dtype, pair);
+    p->pair = pair;
     p->device = dev;
     p->num_sms = sms;
     p->smem_limit = limit;
@@ -600,7 +691,7 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
     p->tiles_n = int((N + block_N - 1) / block_N);
     p->num_tiles = p->tiles_m * p->tiles_n;
     p->grid = p->num_tiles < sms ? p->num_tiles : sms;
-    p->group_m = 8;
+    p->group_m = opts && opts->group_m > 0 ? opts->group_m : 8;
     p->watchdog_ns = env_watchdog();
     p->debug_stall = 0;
     p->maps_valid = false;
@@ -615,6 +706,28 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
         cudaFree(p->d_status);
         delete p;
         return kErrCuda;
+    }
+    if (pair) {
+        // Persistent pairs: as many clusters of two as can be resident at once.
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(unsigned(2 * (p->num_tiles < sms ? p->num_tiles : sms / 2)), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = size_t(p->smem_launch);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, tgemm_kernel<true>, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            cudaFree(p->d_status);
+            delete p;
+            return kErrCuda;
+        }
+        p->grid = 2 * (p->num_tiles < clusters ? p->num_tiles : clusters);
     }
 
     Params &q = p->params;
@@ -634,18 +747,23 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
     q.stages = num_stages;
     q.n_kstep = block_K * L.in_bytes / 32;  // one MMA consumes K = 16 elements = 32 bytes
     q.m_halves = L.m_halves;
+    q.a_rows = L.a_rows;
+    q.b_rows = L.b_rows;
     q.out_mode = out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
     q.acc_stages = L.acc_stages;
     q.acc_cols = L.acc_cols;
     q.tmem_cols = L.tmem_cols;
     // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
     // format (bits 7-9, 10-12: 0 fp16, 1 bf16), both K-major (bits 15, 16 =
-    // 0), N >> 3 (bits 17-22), M >> 4 (bits 24-28) with M = 128.
+    // 0), N >> 3 (bits 17-22), M >> 4 (bits 24-28): M = 128 for one CTA,
+    // M = 256 for the CTA pair.
     const uint32_t ab = dtype == kBF16 ? 1u : 0u;
-    q.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(block_N >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    const uint32_t mma_m = pair ? 256u : 128u;
+    q.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(block_N >> 3) << 17) | ((mma_m >> 4) << 24);
     q.a_slot = round_up(L.a_stage_bytes, kSmemAlign);
     q.b_slot = round_up(L.b_stage_bytes, kSmemAlign);
-    q.stage_tx = L.a_stage_bytes + L.b_stage_bytes;
+    // Bytes that complete one full[s] phase: this CTA's boxes, or both CTAs' in pair mode.
+    q.stage_tx = (L.a_stage_bytes + L.b_stage_bytes) * (pair ? 2u : 1u);
     q.row_bytes = uint32_t(L.swizzle_bytes);
     q.off_a = L.off_a;
     q.off_b = L.off_b;
@@ -676,10 +794,10 @@ static int prepare_maps(tgemm_plan_s *p, const void *A, const void *B, void *C)
     if (p->K > 0) {
         CUtensorMapSwizzle swz = swizzle_for(L.swizzle_bytes);
         rc = encode_2d(&q.tmA, p->dtype, A, uint64_t(p->K), uint64_t(p->M), uint64_t(p->K) * L.in_bytes,
-                       uint32_t(L.bk), uint32_t(L.bm), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                       uint32_t(L.bk), uint32_t(L.a_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (rc == kOk)
             rc = encode_2d(&q.tmB, p->dtype, B, uint64_t(p->K), uint64_t(p->N), uint64_t(p->K) * L.in_bytes,
-                           uint32_t(L.bk), uint32_t(L.bn), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                           uint32_t(L.bk), uint32_t(L.b_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
     if (rc == kOk)
         rc = encode_2d(&q.tmC, p->out_dtype, C, uint64_t(p->N), uint64_t(p->M), uint64_t(p->N) * L.out_bytes,
@@ -706,7 +824,26 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
     if (rc != kOk) return rc;
     p->params.watchdog_ns = p->watchdog_ns;
     p->params.debug_stall = p->debug_stall;
-    tgemm_kernel<<<p->grid, kThreads, p->smem_launch, reinterpret_cast<cudaStream_t>(stream)>>>(p->params);
+    if (p->pair) {
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(unsigned(p->grid), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = size_t(p->smem_launch);
+        cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, tgemm_kernel<true>, p->params) != cudaSuccess) {
+            cudaGetLastError();
+            return kErrCuda;
+        }
+        return kOk;
+    }
+    tgemm_kernel<false><<<p->grid, kThreads, p->smem_launch, reinterpret_cast<cudaStream_t>(stream)>>>(p->params);
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     return kOk;
 }
@@ -788,6 +925,7 @@ int tgemm_get_plan_info(tgemm_plan_t p, tgemm_plan_info *info)
     info->smem_bound = p->L.bound;
     info->smem_limit = p->smem_limit;
     info->num_sms = p->num_sms;
+    info->cta_pair = p->pair;
     return kOk;
 }
 
@@ -911,6 +1049,8 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     q.stages = num_stages;
     q.n_kstep = block_K * L.in_bytes / 32;
     q.m_halves = L.m_halves;
+    q.a_rows = L.a_rows;
+    q.b_rows = L.b_rows;
     q.out_mode = out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
     q.acc_stages = L.acc_stages;
     q.acc_cols = L.acc_cols;
@@ -935,10 +1075,10 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     if (K > 0) {
         const CUtensorMapSwizzle swz = swizzle_for(L.swizzle_bytes);
         rc = encode_2d(&q.tmA, dtype, A, uint64_t(K), uint64_t(M), uint64_t(K) * L.in_bytes, uint32_t(L.bk),
-                       uint32_t(L.bm), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                       uint32_t(L.a_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (rc == kOk)
             rc = encode_2d(&q.tmB, dtype, B, uint64_t(K), uint64_t(N), uint64_t(K) * L.in_bytes, uint32_t(L.bk),
-                           uint32_t(L.bn), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                           uint32_t(L.b_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
     if (rc == kOk)
         rc = encode_2d(&q.tmC, out_dtype, C, uint64_t(N), uint64_t(M), uint64_t(N) * L.out_bytes,
@@ -952,7 +1092,7 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
         cudaGetLastError();
         return kErrCuda;
     }
-    tgemm_kernel<<<grid, kThreads, smem, s>>>(q);
+    tgemm_kernel<false><<<grid, kThreads, smem, s>>>(q);
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     if (status) {
         int h[4] = {0, 0, 0, 0};

@@ -46,9 +46,9 @@ def estimate(M: int, N: int, K: int, block, rel: float, num_sms: int = DEFAULT_S
 
 
 def choose(M: int, N: int, K: int, dtype: int, out_dtype: int, num_sms: int = DEFAULT_SMS):
-    """(block, num_stages) for a problem."""
+    """(block, num_stages, cta_pair) for a problem."""
     hit = FROZEN.get((M, N, K, dtype, out_dtype))
     if hit is not None:
-        return hit
+        return hit[0], hit[1], (hit[2] if len(hit) > 2 else False)
     best = min(CANDIDATES, key=lambda c: (estimate(M, N, K, c[0], c[2], num_sms), -c[2]))
-    return best[0], best[1]
+    return best[0], best[1], False

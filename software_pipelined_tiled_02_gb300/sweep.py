@@ -44,12 +44,15 @@ from software_pipelined_tiled_02_gb300 import inputs  # noqa: E402
 
 PAGES_SPACE = dict(block_M=(64, 128, 256), block_N=(64, 128, 256), block_K=(16, 32, 64), num_stages=(1, 2, 3, 4))
 GB300_SPACE = dict(block_M=(128, 256), block_N=(64, 128, 192, 224, 256), block_K=(32, 64),
-                   num_stages=(2, 3, 4, 5, 6, 8))
+                   num_stages=(2, 3, 4, 5, 6, 8), cta_pair=(0, 1))
 
 
 def enumerate_space(space: dict):
-    keys = ("block_M", "block_N", "block_K", "num_stages")
-    return [dict(zip(keys, v)) for v in itertools.product(*(space[k] for k in keys))]
+    keys = ("block_M", "block_N", "block_K", "num_stages", "cta_pair")
+    vals = [space.get(k, (0,)) for k in keys]
+    out = [dict(zip(keys, v)) for v in itertools.product(*vals)]
+    # CTA pairs exist only for block_M = 256 tiles.
+    return [c for c in out if not (c["cta_pair"] and c["block_M"] != 256)]
 
 
 def prune(configs, M, N, K, dtype, out_dtype, smem_limit, divisible=True):
@@ -61,8 +64,8 @@ def prune(configs, M, N, K, dtype, out_dtype, smem_limit, divisible=True):
         if divisible and (M % c["block_M"] or N % c["block_N"] or K % c["block_K"]):
             rejects["not_divisible"].append(c)
             continue
-        rc = tg.tgemm_validate(M, N, K, dtype, out_dtype, c["block_M"], c["block_N"], c["block_K"],
-                               c["num_stages"], smem_limit)
+        rc = tg.tgemm_validate_ex(M, N, K, dtype, out_dtype, c["block_M"], c["block_N"], c["block_K"],
+                                  c["num_stages"], smem_limit, cta_pair=c.get("cta_pair", 0))
         if rc == tg.OK:
             legal.append(c)
         elif rc == tg.ERR_SMEM_BUDGET:
@@ -132,7 +135,7 @@ class Runner:
         row = dict(c)
         try:
             plan = tg.Plan(self.M, self.N, self.K, w["dtype"], w["out"],
-                           (c["block_M"], c["block_N"], c["block_K"]), c["num_stages"])
+                           (c["block_M"], c["block_N"], c["block_K"]), c["num_stages"], pair=bool(c.get("cta_pair")))
         except tg.TgemmError as e:
             row.update(ok=False, error=str(e))
             return row
@@ -230,8 +233,8 @@ def main(argv=None):
         best = pick_best(rows)
         report["best"] = best
         for r in sorted(rows, key=lambda r: r.get("median_ms", 1e9))[:10]:
-            print(json.dumps({k: r[k] for k in ("block_M", "block_N", "block_K", "num_stages", "median_ms",
-                                                "tflops", "smem_bytes", "ok")}), flush=True)
+            print(json.dumps({k: r.get(k) for k in ("block_M", "block_N", "block_K", "num_stages", "cta_pair",
+                                                    "median_ms", "tflops", "smem_bytes", "ok")}), flush=True)
         if best and not args.no_cache:
             path = cache_path(dev, args.workload)
             os.makedirs(os.path.dirname(path), exist_ok=True)

@@ -24,10 +24,10 @@ def to_dev(bits, dtype):
     return inputs.bits_to_torch(bits, dtype).cuda()
 
 
-def run(tg, A, B, dtype, out, block, stages):
+def run(tg, A, B, dtype, out, block, stages, pair=False):
     M, K = A.shape
     N = B.shape[0]
-    plan = tg.Plan(M, N, K, dtype, out, block, stages)
+    plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair)
     dA, dB = to_dev(A, dtype), to_dev(B, dtype)
     C = torch.full((M, N), float("nan"), dtype=TORCH[out], device="cuda")
     plan.run(dA, dB, C)
@@ -88,6 +88,64 @@ def test_integer_inputs_bit_exact(cuda_lib, block, stages, dtype):
     C = as_f64(run(cuda_lib, A, B, dtype, "f32", block, stages))
     R, _ = oracle.gemm(A, B, dtype)
     assert np.array_equal(C, R)
+
+
+# ------------------------------------------------------------ CTA-pair mode
+
+PAIR_CONFIGS = [
+    ((256, 256, 64), 4),
+    ((256, 224, 64), 6),
+    ((256, 128, 32), 3),
+    ((256, 64, 16), 2),
+    ((256, 32, 64), 1),
+]
+
+
+@pytest.mark.parametrize("block,stages", PAIR_CONFIGS, ids=lambda v: str(v))
+@pytest.mark.parametrize("shape", SHAPES + [(520, 704, 264)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("bf16", "bf16"), ("f16", "f16")])
+def test_pair_small_shapes(cuda_lib, block, stages, shape, dtype, out):
+    M, N, K = shape
+    A, B = inputs.operands(200 + M + N + K, M, N, K, dtype, "uniform")
+    C = as_f64(run(cuda_lib, A, B, dtype, out, block, stages, pair=True))
+    R, S = oracle.gemm(A, B, dtype)
+    assert_close(C, R, S, out)
+
+
+@pytest.mark.parametrize("block,stages", PAIR_CONFIGS, ids=lambda v: str(v))
+def test_pair_integer_inputs_bit_exact(cuda_lib, block, stages):
+    M, N, K = 600, 520, 2056
+    A, B = inputs.operands(41, M, N, K, "bf16", "int", lo=-4, hi=4)
+    C = as_f64(run(cuda_lib, A, B, "bf16", "f32", block, stages, pair=True))
+    R, _ = oracle.gemm(A, B, "bf16")
+    assert np.array_equal(C, R)
+
+
+def test_pair_matches_single_cta_bitwise(cuda_lib):
+    # The pair issues the same K-ordered MMAs over the same tile as one CTA
+    # with two M-halves; the fp32 accumulation must come out bit for bit.
+    M, N, K = 1024, 1024, 1024
+    A, B = inputs.operands(42, M, N, K, "f16", "normal")
+    one = run(cuda_lib, A, B, "f16", "f32", (256, 128, 64), 3, pair=False)
+    two = run(cuda_lib, A, B, "f16", "f32", (256, 128, 64), 3, pair=True)
+    assert torch.equal(one.view(torch.int32), two.view(torch.int32))
+
+
+def test_pair_rejects_other_block_m(cuda_lib):
+    rc, h = cuda_lib.tgemm_plan_ex(512, 512, 512, "f16", "f32", 128, 128, 64, 3, cta_pair=1)
+    assert rc == cuda_lib.ERR_NO_KERNEL and h is None
+    rc, h = cuda_lib.tgemm_plan_ex(512, 512, 512, "f16", "f32", 256, 128, 64, 3, cta_pair=2)
+    assert rc == cuda_lib.ERR_INVALID_ARG and h is None
+
+
+@pytest.mark.parametrize("name,block,stages", [("gemm_4096_f16_normal", (256, 256, 64), 6),
+                                               ("gemm_8192_bf16_normal", (256, 224, 64), 6)])
+def test_pair_full_size_sampled(cuda_lib, name, block, stages):
+    w, A, B, C = full_size(cuda_lib, name, block, stages, pair=True)
+    rows, cols = sample_entries(w["M"], w["N"], 4096, 6)
+    R, S = oracle.gemm_entries(A, B, w["dtype"], rows, cols)
+    got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+    assert_close(as_f64(got), R, S, w["out"])
 
 
 # ------------------------------------------------------------ degenerate cases
@@ -195,12 +253,12 @@ def sample_entries(M, N, n_random, seed):
     return np.concatenate(rows), np.concatenate(cols)
 
 
-def full_size(cuda_lib, name, block=None, stages=None):
+def full_size(cuda_lib, name, block=None, stages=None, pair=False):
     w = inputs.WORKLOADS[name]
     A, B = inputs.workload_operands(name)
     if block is None:
-        block, stages = cuda_lib.default_config(w["M"], w["N"], w["K"], w["dtype"], w["out"])
-    C = run(cuda_lib, A, B, w["dtype"], w["out"], block, stages)
+        block, stages, pair = cuda_lib.default_config(w["M"], w["N"], w["K"], w["dtype"], w["out"])
+    C = run(cuda_lib, A, B, w["dtype"], w["out"], block, stages, pair)
     return w, A, B, C
 
 

@@ -18,14 +18,14 @@ def bits(C):
     return C.view(torch.int32 if C.element_size() == 4 else torch.int16)
 
 
-def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed):
+def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=False):
     A, B = inputs.operands(seed, M, N, K, dtype, "normal")
     dA = inputs.bits_to_torch(A, dtype).cuda()
     dB = inputs.bits_to_torch(B, dtype).cuda()
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[out]
     res = []
     for s in stage_list:
-        plan = tg.Plan(M, N, K, dtype, out, block, s)
+        plan = tg.Plan(M, N, K, dtype, out, block, s, pair=pair)
         C = torch.full((M, N), float("nan"), dtype=tdt, device="cuda")
         plan.run(dA, dB, C)
         torch.cuda.synchronize()
@@ -52,3 +52,10 @@ def test_bit_identical_across_stages_4096(cuda_lib):
     res = outputs_over_stages(cuda_lib, 4096, 4096, 4096, "f16", "f16", (128, 128, 32), (1, 2, 3, 4, 6), seed=2)
     for C in res[1:]:
         assert torch.equal(bits(C), bits(res[0]))
+
+
+@pytest.mark.parametrize("block,stage_list", [((256, 256, 64), (1, 2, 4, 6)), ((256, 128, 32), (1, 3, 8))])
+def test_bit_identical_across_stages_pair(cuda_lib, block, stage_list):
+    res = outputs_over_stages(cuda_lib, 1000, 1040, 2056, "bf16", "f32", block, stage_list, seed=78, pair=True)
+    for s, C in zip(stage_list[1:], res[1:]):
+        assert torch.equal(bits(C), bits(res[0])), f"num_stages={s} differs"

@@ -16,6 +16,7 @@ def setup_module(_):
 def test_pages_space_prunes_over_budget_before_launch():
     cfgs = sweep.enumerate_space(sweep.PAGES_SPACE)
     assert len(cfgs) == 3 * 3 * 3 * 4  # the pages' grid without its `threads` axis
+    assert all(c["cta_pair"] == 0 for c in cfgs)
     legal, rej = sweep.prune(cfgs, 4096, 4096, 4096, tg.F16, tg.F16, LIMIT)
     over = {(c["block_M"], c["block_N"], c["block_K"], c["num_stages"]) for c in rej["smem_budget"]}
     assert (256, 256, 64, 4) in over
@@ -60,3 +61,14 @@ def test_cache_switch(tmp_path, monkeypatch):
     assert sweep.load_cached("NVIDIA GB300", "wl") == {"block_M": 256}
     monkeypatch.setenv("TGEMM_AUTOTUNE_DISABLE_CACHE", "1")
     assert sweep.load_cached("NVIDIA GB300", "wl") is None
+
+
+def test_gb300_space_has_pairs_only_for_256_rows():
+    cfgs = sweep.enumerate_space(sweep.GB300_SPACE)
+    pairs = [c for c in cfgs if c["cta_pair"]]
+    assert pairs and all(c["block_M"] == 256 for c in pairs)
+    legal, rej = sweep.prune(cfgs, 4096, 4096, 4096, tg.F16, tg.F16, LIMIT, divisible=False)
+    # A pair CTA holds half of B: 256x256x64 fits 6 stages as a pair, 3 alone.
+    key = lambda c: (c["block_M"], c["block_N"], c["block_K"], c["num_stages"], c["cta_pair"])  # noqa: E731
+    ok = {key(c) for c in legal}
+    assert (256, 256, 64, 6, 1) in ok and (256, 256, 64, 6, 0) not in ok and (256, 256, 64, 3, 0) in ok

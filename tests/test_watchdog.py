@@ -16,14 +16,15 @@ from software_pipelined_tiled_02_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("block,stages", [((128, 128, 32), 3), ((128, 256, 64), 1)])
-def test_stall_reports_timeout_and_context_survives(cuda_lib, block, stages):
+@pytest.mark.parametrize("block,stages,pair", [((128, 128, 32), 3, False), ((128, 256, 64), 1, False),
+                                               ((256, 256, 64), 4, True)])
+def test_stall_reports_timeout_and_context_survives(cuda_lib, block, stages, pair):
     M, N, K = 512, 512, 512
     A, B = inputs.operands(31, M, N, K, "f16", "uniform")
     dA = inputs.bits_to_torch(A, "f16").cuda()
     dB = inputs.bits_to_torch(B, "f16").cuda()
     C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
-    plan = cuda_lib.Plan(M, N, K, "f16", "f32", block, stages)
+    plan = cuda_lib.Plan(M, N, K, "f16", "f32", block, stages, pair=pair)
     plan.set_watchdog_ns(50_000_000)
     plan.debug_stall(True)
     plan.run(dA, dB, C)
