@@ -22,10 +22,9 @@ enum : int {
 
 enum : int { kF16 = 0, kBF16 = 1, kF32 = 2 };
 
-constexpr int kThreads = 192;         // 6 warps: TMA producer, MMA issuer, 4 epilogue warps
-constexpr int kEpiWarps = 4;
+constexpr int kThreads = 320;         // 10 warps: TMA producer, MMA issuer, 8 epilogue warps
+constexpr int kEpiWarps = 8;          // two per TMEM lane quarter, splitting the column chunks
 constexpr int kEpiCols = 32;          // accumulator columns per epilogue chunk
-constexpr int kEpiBufs = 2;           // staging buffers per epilogue warp
 constexpr int kTmemColsMax = 512;     // tensor-memory columns per SM
 constexpr uint32_t kSmemAlign = 1024; // swizzle-atom alignment of every tile slot
 
@@ -39,6 +38,7 @@ struct Layout {
     uint32_t a_stage_bytes;  // bm * bk * in_bytes
     uint32_t b_stage_bytes;  // bn * bk * in_bytes
     uint32_t c_buf_bytes;    // one staging buffer: 32 rows x kEpiCols x out_bytes
+    int epi_bufs;            // staging buffers per epilogue warp: 2 for 16-bit C, 1 for fp32 C
     uint32_t off_a, off_b, off_c, off_bar;
     uint32_t bar_bytes;
     uint32_t total;          // bytes requested, including alignment slack
@@ -87,10 +87,11 @@ inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out
     // The pages' bound for the operand tiles one CTA (one block) holds.
     L.bound = int64_t(stages) * (int64_t(L.a_rows) * bk + int64_t(bk) * L.b_rows) * L.in_bytes;
     L.c_buf_bytes = 32u * kEpiCols * L.out_bytes;
+    L.epi_bufs = L.out_bytes == 4 ? 1 : 2;
     L.off_a = 0;
     L.off_b = L.off_a + uint32_t(stages) * round_up(L.a_stage_bytes, kSmemAlign);
     L.off_c = L.off_b + uint32_t(stages) * round_up(L.b_stage_bytes, kSmemAlign);
-    L.off_bar = L.off_c + round_up(uint32_t(kEpiWarps * kEpiBufs) * L.c_buf_bytes, kSmemAlign);
+    L.off_bar = L.off_c + round_up(uint32_t(kEpiWarps * L.epi_bufs) * L.c_buf_bytes, kSmemAlign);
     L.bar_bytes = barrier_block_bytes(stages);
     L.total = L.off_bar + L.bar_bytes + kSmemAlign;  // slack to align the dynamic base
     L.m_halves = pair ? 1 : bm / 128;

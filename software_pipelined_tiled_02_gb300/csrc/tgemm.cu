@@ -70,6 +70,7 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     uint32_t stage_tx;          // bytes the TMA delivers per slot (A box + B box)
     uint32_t row_bytes;         // bytes of one K-contiguous operand row in a slot
     uint32_t off_a, off_b, off_c, off_bar, c_buf_bytes;
+    int epi_bufs;               // staging buffers per epilogue warp (1 or 2)
     uint32_t desc_lo_flags;     // leading-byte-offset field of the smem descriptor
     uint32_t desc_hi;           // high word: stride byte offset, version, swizzle mode
     unsigned long long watchdog_ns;
@@ -387,10 +388,13 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                 mma_dispatch_nk<1, PAIR>(p, c, abort, lane);
         }
     } else {
-        // ---------------- epilogue: 4 warps, warp w reads TMEM lanes 32*(w%4)..+31
+        // ---------------- epilogue: 8 warps; warp w reads TMEM lanes 32*(w%4)..+31,
+        // and the two warps of a lane quarter take alternate 32-column chunks.
         const int q = warp & 3;
+        const int sub = (warp - 2) >> 2;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
-        const uint32_t my_bufs = sC + uint32_t((warp - 2) * kEpiBufs) * p.c_buf_bytes;
+        const int nbuf = p.epi_bufs;
+        const uint32_t my_bufs = sC + uint32_t((warp - 2) * nbuf) * p.c_buf_bytes;
         int a = 0;
         uint32_t aph = 0;
         uint32_t chunk = 0;
@@ -401,12 +405,14 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
             const int m0 = mb * p.bm + int(rank) * p.a_rows, n0 = nb * p.bn;
             if (!warp_wait(acc_full(a), aph, p, abort, 2, tiles_done)) break;
             tc_fence_after();
+            int idx = 0;
             for (int h = 0; h < p.m_halves; ++h) {
                 const int row0 = m0 + h * 128 + q * 32;
                 if (row0 >= p.M) continue;  // warp-uniform
                 for (int c = 0; c * kEpiCols < p.bn; ++c) {
                     const int col0 = n0 + c * kEpiCols;
                     if (col0 >= p.N) break;  // warp-uniform
+                    if ((idx++ & 1) != sub) continue;  // the other warp of this quarter takes it
                     uint32_t v[32];
                     if (p.num_kb > 0) {
                         tmem_ld_32x32b_x32(tmem + lane_base + uint32_t(a * p.acc_cols + h * p.bn + c * kEpiCols), v);
@@ -415,8 +421,13 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0u;  // empty reduction
                     }
-                    const uint32_t buf = my_bufs + (chunk & 1u) * p.c_buf_bytes;
-                    if (chunk >= 2 && lane == 0) bulk_wait_read<1>();  // buffer's previous store has read it
+                    const uint32_t buf = my_bufs + (nbuf == 2 ? (chunk & 1u) : 0u) * p.c_buf_bytes;
+                    if (chunk >= uint32_t(nbuf) && lane == 0) {  // buffer's previous store has read it
+                        if (nbuf == 2)
+                            bulk_wait_read<1>();
+                        else
+                            bulk_wait_read<0>();
+                    }
                     __syncwarp();
                     if (p.out_mode == 0) {
                         // fp32: 128-byte rows, 128-byte swizzle (16-byte chunk j of row r at j ^ (r % 8))
@@ -770,6 +781,7 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     q.off_c = L.off_c;
     q.off_bar = L.off_bar;
     q.c_buf_bytes = L.c_buf_bytes;
+    q.epi_bufs = L.epi_bufs;
     // Leading byte offset is unused for swizzled K-major tiles whose K extent
     // per MMA lies inside one swizzle row; encode 16 bytes.  Stride byte
     // offset: 8 rows of one swizzle span each.
@@ -1066,6 +1078,7 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     q.off_c = L.off_c;
     q.off_bar = L.off_bar;
     q.c_buf_bytes = L.c_buf_bytes;
+    q.epi_bufs = L.epi_bufs;
     q.desc_lo_flags = (1u << 16);
     const uint32_t sbo = 8u * uint32_t(L.swizzle_bytes);
     q.desc_hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (desc_layout_for(L.swizzle_bytes) << 29);
