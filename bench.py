@@ -52,6 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--stages", type=int, default=None)
     ap.add_argument("--pair", type=int, choices=(0, 1), default=None,
                     help="1: CTA pairs (clusters of 2) share each 256-row tile (default: tuned table)")
+    ap.add_argument("--split-k", type=int, default=None, help="K splits per tile (default: tuned table)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -286,19 +287,23 @@ def run_ours(args, w, world, rank, local):
         block = tuple(int(x) for x in args.block.split(","))
         stages = args.stages or 4
         pair = bool(args.pair)
+        split_k = args.split_k or 1
     else:
-        block, stages, pair = tg.default_config(M, N, K, w["dtype"], w["out"])
+        cfg = tg.default_config(M, N, K, w["dtype"], w["out"])
+        block, stages, pair, split_k = cfg["block"], cfg["num_stages"], cfg["cta_pair"], cfg["split_k"]
         if args.stages:
             stages = args.stages
         if args.pair is not None:
             pair = bool(args.pair)
+        if args.split_k is not None:
+            split_k = args.split_k
     A, B = inputs.workload_operands(args.workload)
     hA = inputs.bits_to_torch(A, w["dtype"])
     hB = inputs.bits_to_torch(B, w["dtype"])
     dA, dB = hA.to(dev), hB.to(dev)
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[w["out"]]
     dC = torch.empty((M, N), dtype=tdt, device=dev)
-    plan = tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair)
+    plan = tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k)
     info = plan.info
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -391,9 +396,10 @@ def run_ours(args, w, world, rank, local):
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": max_mean_ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
-                "config": dict(config_block(args, w, block, stages), cta_pair=int(pair)), "roofline": roofline,
+                "config": dict(config_block(args, w, block, stages), cta_pair=int(pair),
+                               split_k=int(info["split_k"])), "roofline": roofline,
                 "cpu_baseline": cpu,
-                "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
+                "e2e": e2e, "gpu_launches": args.steps * (2 if info["split_k"] > 1 else 1), "clocks": clocks,
                 "plan": {k: info[k] for k in ("grid", "num_tiles", "smem_bytes", "tmem_columns", "acc_stages")},
                 "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms), "max": max(kernel_ms)}}
     plan.close()

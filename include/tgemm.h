@@ -130,10 +130,20 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
  *     block in the sense of the pages' budget rule: the bound checked is
  *     num_stages x (128 x block_K + block_K x block_N / 2) x element size.
  *   group_m: M-tiles per raster group of the persistent schedule (0: 8).
+ *   split_k: 0 or 1 = no split.  s > 1 = split the K loop of every tile into
+ *     s ranges of whole k-blocks (fewer if K has fewer k-blocks), computed as
+ *     separate work units that write fp32 partial tiles to a workspace of
+ *     s x ceil(M / block_M) x block_M x N floats the plan allocates; a second
+ *     kernel then adds the partials in split order (0, 1, ..., s-1) and
+ *     rounds once to C's type.
+ *     The order of every sum depends only on the tile shape and s, never on
+ *     num_stages, so results stay bit-identical across depths.  For long K
+ *     and few output tiles (more SMs than tiles).  At most 64.
  */
 typedef struct tgemm_plan_opts {
     int cta_pair;
     int group_m;
+    int split_k;
 } tgemm_plan_opts;
 
 /* tgemm_validate with options (NULL = defaults). */
@@ -206,6 +216,8 @@ typedef struct tgemm_plan_info {
     int smem_limit;      /* device per-block limit at plan time */
     int num_sms;
     int cta_pair;        /* 1: clusters of two CTAs share each tile */
+    int split_k;         /* effective K splits (1: none) */
+    int num_units;       /* persistent work units: tiles x K splits */
 } tgemm_plan_info;
 
 int tgemm_get_plan_info(tgemm_plan_t plan, tgemm_plan_info *info);

@@ -45,14 +45,14 @@ class PlanInfo(ctypes.Structure):
                 ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("num_k_blocks", ctypes.c_int),
                 ("acc_stages", ctypes.c_int), ("tmem_columns", ctypes.c_int), ("smem_bytes", ctypes.c_int64),
                 ("smem_bound", ctypes.c_int64), ("smem_limit", ctypes.c_int), ("num_sms", ctypes.c_int),
-                ("cta_pair", ctypes.c_int)]
+                ("cta_pair", ctypes.c_int), ("split_k", ctypes.c_int), ("num_units", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class PlanOpts(ctypes.Structure):
-    _fields_ = [("cta_pair", ctypes.c_int), ("group_m", ctypes.c_int)]
+    _fields_ = [("cta_pair", ctypes.c_int), ("group_m", ctypes.c_int), ("split_k", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -151,18 +151,19 @@ def tgemm_plan(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages)
     return int(rc), (h if rc == OK else None)
 
 
-def tgemm_plan_ex(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, cta_pair=0, group_m=0):
+def tgemm_plan_ex(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, cta_pair=0, group_m=0,
+                  split_k=0):
     """Returns ``(status, handle)``; handle is None on failure."""
     h = ctypes.c_void_p()
-    opts = PlanOpts(int(cta_pair), int(group_m))
+    opts = PlanOpts(int(cta_pair), int(group_m), int(split_k))
     rc = load().tgemm_plan_ex(ctypes.byref(h), M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K,
                               num_stages, ctypes.byref(opts))
     return int(rc), (h if rc == OK else None)
 
 
 def tgemm_validate_ex(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit, cta_pair=0,
-                      group_m=0) -> int:
-    opts = PlanOpts(int(cta_pair), int(group_m))
+                      group_m=0, split_k=0) -> int:
+    opts = PlanOpts(int(cta_pair), int(group_m), int(split_k))
     return int(load().tgemm_validate_ex(M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K,
                                         num_stages, smem_limit, ctypes.byref(opts)))
 
@@ -225,18 +226,21 @@ tgemm_strerror = strerror
 class Plan:
     """A validated GEMM configuration on the current CUDA device."""
 
-    def __init__(self, M, N, K, dtype="f16", out_dtype=None, block=(128, 256, 64), num_stages=4, pair=False):
+    def __init__(self, M, N, K, dtype="f16", out_dtype=None, block=(128, 256, 64), num_stages=4, pair=False,
+                 split_k=1):
         dtype = _dt(dtype)
         out_dtype = dtype if out_dtype is None else _dt(out_dtype)
         bm, bn, bk = block
-        if pair:
-            rc, h = tgemm_plan_ex(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages, cta_pair=1)
+        if pair or split_k > 1:
+            rc, h = tgemm_plan_ex(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages, cta_pair=int(bool(pair)),
+                                  split_k=int(split_k))
         else:
             rc, h = tgemm_plan(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages)
         if rc != OK:
             raise TgemmError(rc, f"tgemm_plan(M={M}, N={N}, K={K}, block={block}, num_stages={num_stages}, "
-                                 f"pair={pair})")
+                                 f"pair={pair}, split_k={split_k})")
         self.pair = bool(pair)
+        self.split_k = int(split_k)
         self.handle = h
         self.M, self.N, self.K = M, N, K
         self.dtype, self.out_dtype = dtype, out_dtype
@@ -311,14 +315,14 @@ class Plan:
 _plans: dict = {}
 
 
-def default_config(M, N, K, dtype="f16", out_dtype=None):
-    """The tuned default (block, num_stages, cta_pair) for a shape."""
+def default_config(M, N, K, dtype="f16", out_dtype=None) -> dict:
+    """The tuned default {block, num_stages, cta_pair, split_k} for a shape."""
     from . import defaults
 
     return defaults.choose(M, N, K, _dt(dtype), _dt(dtype) if out_dtype is None else _dt(out_dtype))
 
 
-def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=None, pair=None):
+def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=None, pair=None, split_k=None):
     """``A[M,K] . B[N,K]^T`` on the GPU through ``libtgemm.so``.
 
     ``out_dtype`` defaults to the operand dtype; ``torch.float32`` returns the
@@ -331,13 +335,15 @@ def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=Non
     dt = _dt(A.dtype)
     odt = dt if out_dtype is None else _dt(out_dtype)
     if block is None or num_stages is None:
-        b, s, pr = default_config(M, N, K, dt, odt)
-        block = block or b
-        num_stages = num_stages or s
-        pair = pr if pair is None else pair
+        cfg = default_config(M, N, K, dt, odt)
+        block = block or cfg["block"]
+        num_stages = num_stages or cfg["num_stages"]
+        pair = cfg["cta_pair"] if pair is None else pair
+        split_k = cfg["split_k"] if split_k is None else split_k
     pair = bool(pair)
-    key = (M, N, K, dt, odt, tuple(block), num_stages, pair, A.device.index)
+    split_k = int(split_k or 1)
+    key = (M, N, K, dt, odt, tuple(block), num_stages, pair, split_k, A.device.index)
     plan = _plans.get(key)
     if plan is None:
-        plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages, pair=pair)
+        plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages, pair=pair, split_k=split_k)
     return plan.run(A, B, out, stream)

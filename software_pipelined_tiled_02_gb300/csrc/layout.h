@@ -106,8 +106,20 @@ inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out
 }
 
 // Every check of tgemm_validate, in the documented order.
+// Largest number of K splits a plan accepts.
+constexpr int kMaxSplits = 64;
+
+// Effective number of K splits: at least one k-block per split.
+inline int effective_splits(int64_t K, int bk, int splits)
+{
+    const int64_t kb = (K + bk - 1) / bk;
+    if (splits <= 1 || kb <= 1) return 1;
+    const int64_t per = (kb + splits - 1) / splits;
+    return int((kb + per - 1) / per);
+}
+
 inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int bm, int bn, int bk,
-                    int stages, int64_t smem_limit, int pair = 0)
+                    int stages, int64_t smem_limit, int pair = 0, int splits = 1)
 {
     if (dtype != kF16 && dtype != kBF16) return kErrUnsupportedDtype;
     if (out_dtype != kF32 && out_dtype != dtype) return kErrUnsupportedDtype;
@@ -117,8 +129,11 @@ inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, i
     if ((K * dtype_bytes(dtype)) % 16 != 0) return kErrAlignment;
     if ((N * dtype_bytes(out_dtype)) % 16 != 0) return kErrAlignment;
     if (!tile_supported(bm, bn, bk, dtype_bytes(dtype), pair)) return kErrNoKernel;
+    if (splits < 1 || splits > kMaxSplits) return kErrInvalidArg;
     if (stages > 64) return kErrSmemBudget;  // keeps the layout arithmetic in 32 bits
-    Layout L = make_layout(bm, bn, bk, stages, dtype, out_dtype, pair);
+    // A split-K kernel stages fp32 partial tiles whatever the final output type.
+    const int staged = effective_splits(K, bk, splits) > 1 ? kF32 : out_dtype;
+    Layout L = make_layout(bm, bn, bk, stages, dtype, staged, pair);
     if (L.bound > smem_limit || int64_t(L.total) > smem_limit) return kErrSmemBudget;
     return kOk;
 }

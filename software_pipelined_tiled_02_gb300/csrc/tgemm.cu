@@ -59,6 +59,10 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     int M, N, K;
     int num_kb;                 // ceil(K / bk)
     int tiles_m, tiles_n, num_tiles, group_m;
+    int splits, kb_per_split;   // K splits per tile (1: none) and k-blocks per split
+    int split_rows;             // workspace rows per split: tiles_m * block_M, so a tile's
+                                // ragged tail stays inside its own split's rows
+    int num_units;              // work units: num_tiles * splits
     int bm, bn, bk, stages;
     int n_kstep;                // bk / 16 MMAs along K per slot
     int m_halves;               // bm / 128 (1 in pair mode: one M = 256 MMA covers both CTAs)
@@ -135,6 +139,25 @@ __device__ __forceinline__ void tile_coords(const Params &p, int t, int &m_blk, 
     n_blk = r / gm;
 }
 
+// Work unit u = (tile, K split): its tile, its k-block range [kb0, kb1) and
+// the row offset of its output (split s writes rows s*R .. s*R+R-1 of the
+// partial-sum workspace, R = tiles_m * block_M >= M; 0 without splitting).
+struct Unit {
+    int mb, nb, kb0, kb1, row_off;
+};
+
+__device__ __forceinline__ Unit unit_coords(const Params &p, int u)
+{
+    Unit w;
+    const int tile = u / p.splits;
+    const int split = u - tile * p.splits;
+    tile_coords(p, tile, w.mb, w.nb);
+    w.kb0 = split * p.kb_per_split;
+    w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
+    w.row_off = split * p.split_rows;
+    return w;
+}
+
 // Shared-memory matrix descriptor of a K-major swizzled operand tile starting
 // at shared address `addr` (bits 0-13: address >> 4; 16-29: leading byte
 // offset >> 4; 32-45: stride byte offset >> 4; 46: version 1; 61-63: swizzle).
@@ -188,19 +211,21 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
     int it = 0;
     bool ok = true;
     if (p.debug_stall) ok = warp_wait(c.stall, 0, p, abort, 1, 0);  // test hook: nothing arrives
-    for (int t = c.unit0; ok && t < p.num_tiles; t += c.ustride) {
+    for (int t = c.unit0; ok && t < p.num_units; t += c.ustride) {
+        const int kb0 = (t - (t / p.splits) * p.splits) * p.kb_per_split;
+        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         if (!warp_wait(acc_empty(a), aph ^ 1u, p, abort, 1, it)) break;
         tc_fence_after();
         const uint32_t d = c.tmem + uint32_t(a * p.acc_cols);
         const uint32_t d2 = d + uint32_t(p.bn);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
             if (!warp_wait(full(s), ph, p, abort, 1, it)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t first = kb != 0 ? 1u : 0u;
+                const uint32_t first = kb != kb0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < NK; ++kk) {
 #pragma unroll
@@ -331,11 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         uint32_t ph = 0;
         int issued = 0;
         bool ok = true;
-        for (int t = unit0; ok && t < p.num_tiles; t += ustride) {
-            int mb, nb;
-            tile_coords(p, t, mb, nb);
-            const int m0 = mb * p.bm + int(rank) * p.a_rows, n0 = nb * p.bn + int(rank) * p.b_rows;
-            for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int t = unit0; ok && t < p.num_units; t += ustride) {
+            const Unit w = unit_coords(p, t);
+            const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn + int(rank) * p.b_rows;
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 if (!warp_wait(empty(s), ph ^ 1u, p, abort, 0, issued)) {
                     ok = false;
                     break;
@@ -399,10 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         uint32_t aph = 0;
         uint32_t chunk = 0;
         int tiles_done = 0;
-        for (int t = unit0; t < p.num_tiles; t += ustride, ++tiles_done) {
-            int mb, nb;
-            tile_coords(p, t, mb, nb);
-            const int m0 = mb * p.bm + int(rank) * p.a_rows, n0 = nb * p.bn;
+        for (int t = unit0; t < p.num_units; t += ustride, ++tiles_done) {
+            const Unit w = unit_coords(p, t);
+            const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn;
             if (!warp_wait(acc_full(a), aph, p, abort, 2, tiles_done)) break;
             tc_fence_after();
             int idx = 0;
@@ -460,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tmC, col0, row0, buf);
+                        tma_store_2d(&p.tmC, col0, w.row_off + row0, buf);
                         bulk_commit();
                     }
                     ++chunk;
@@ -494,6 +517,42 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
             tmem_dealloc_pair(tmem, uint32_t(p.tmem_cols));
         else
             tmem_dealloc(tmem, uint32_t(p.tmem_cols));
+    }
+}
+
+// Split-K reduction: C[i] = sum over s = 0, 1, ..., splits-1 (in that order)
+// of the fp32 partials W[s * stride + i], rounded once to the output type.
+// Elementwise and HBM-bound: four consecutive elements per thread per step
+// (M*N and the split stride are multiples of 4 because every row pitch is a
+// multiple of 16 bytes).
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ W, void *__restrict__ C,
+                                                            int64_t mn, int64_t stride, int splits, int out_mode)
+{
+    const int64_t n4 = mn / 4;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
+        float4 acc = reinterpret_cast<const float4 *>(W)[i];
+        for (int s = 1; s < splits; ++s) {
+            const float4 v = reinterpret_cast<const float4 *>(W + int64_t(s) * stride)[i];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        if (out_mode == 0) {
+            reinterpret_cast<float4 *>(C)[i] = acc;
+        } else if (out_mode == 1) {
+            __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            reinterpret_cast<uint2 *>(C)[i] = u;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            reinterpret_cast<uint2 *>(C)[i] = u;
+        }
     }
 }
 
@@ -563,6 +622,8 @@ struct tgemm_plan_s {
     int smem_launch;
     int tiles_m, tiles_n, num_tiles, grid, group_m;
     int pair;  // clusters of two CTAs per block_M = 256 tile
+    int splits;                // K splits (1: none)
+    float *d_work;             // split-K partial sums, splits x M x N fp32 (owned by the plan)
     int *d_status;
     unsigned long long watchdog_ns;
     int debug_stall;
@@ -647,7 +708,7 @@ int tgemm_validate_ex(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
                       int block_K, int num_stages, int64_t smem_limit, const tgemm_plan_opts *opts)
 {
     return validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit,
-                    opts ? opts->cta_pair : 0);
+                    opts ? opts->cta_pair : 0, opts && opts->split_k > 1 ? opts->split_k : 1);
 }
 
 int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N,
@@ -664,8 +725,10 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     const int pair = opts && opts->cta_pair ? 1 : 0;
     if (opts && (opts->cta_pair != 0 && opts->cta_pair != 1)) return kErrInvalidArg;
     if (opts && (opts->group_m < 0 || opts->group_m > 4096)) return kErrInvalidArg;
+    if (opts && (opts->split_k < 0 || opts->split_k > kMaxSplits)) return kErrInvalidArg;
+    const int splits = effective_splits(K, block_K, opts && opts->split_k > 1 ? opts->split_k : 1);
     // Argument checks that need no device come first.
-    int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX, pair);
+    int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX, pair, splits);
     if (rc != kOk) return rc;
     int dev = 0, major = 0, minor = 0, sms = 0, limit = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
@@ -677,7 +740,7 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
         return kErrCuda;
     }
     if (major != 10 || minor != 3) return kErrArch;
-    rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit, pair);
+    rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit, pair, splits);
     if (rc != kOk) return rc;
 
     tgemm_plan_s *p = new (std::nothrow) tgemm_plan_s();
@@ -687,8 +750,11 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     p->K = K;
     p->dtype = dtype;
     p->out_dtype = out_dtype;
-    p->L = make_layout(block_M, block_N, block_K, num_stages, dtype, out_dtype, pair);
+    // With K splits the kernel stages fp32 partial tiles; the reduction converts.
+    p->L = make_layout(block_M, block_N, block_K, num_stages, dtype, splits > 1 ? kF32 : out_dtype, pair);
     p->pair = pair;
+    p->splits = splits;
+    p->d_work = nullptr;
     p->device = dev;
     p->num_sms = sms;
     p->smem_limit = limit;
@@ -701,7 +767,8 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     p->tiles_m = int((M + block_M - 1) / block_M);
     p->tiles_n = int((N + block_N - 1) / block_N);
     p->num_tiles = p->tiles_m * p->tiles_n;
-    p->grid = p->num_tiles < sms ? p->num_tiles : sms;
+    const int units = p->num_tiles * splits;
+    p->grid = units < sms ? units : sms;
     p->group_m = opts && opts->group_m > 0 ? opts->group_m : 8;
     p->watchdog_ns = env_watchdog();
     p->debug_stall = 0;
@@ -726,7 +793,7 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(unsigned(2 * (p->num_tiles < sms ? p->num_tiles : sms / 2)), 1, 1);
+        cfg.gridDim = dim3(unsigned(2 * (units < sms / 2 ? units : sms / 2)), 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = size_t(p->smem_launch);
         cfg.attrs = attr;
@@ -738,7 +805,16 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
             delete p;
             return kErrCuda;
         }
-        p->grid = 2 * (p->num_tiles < clusters ? p->num_tiles : clusters);
+        p->grid = 2 * (units < clusters ? units : clusters);
+    }
+    if (splits > 1) {
+        const size_t bytes = size_t(splits) * size_t(p->tiles_m) * size_t(block_M) * size_t(N) * sizeof(float);
+        if (cudaMalloc(&p->d_work, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(p->d_status);
+            delete p;
+            return kErrCuda;
+        }
     }
 
     Params &q = p->params;
@@ -752,6 +828,11 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     q.tiles_n = p->tiles_n;
     q.num_tiles = p->num_tiles;
     q.group_m = p->group_m;
+    q.splits = splits;
+    // effective_splits guarantees every split a non-empty k-block range
+    q.kb_per_split = splits > 1 ? (q.num_kb + splits - 1) / splits : q.num_kb;
+    q.num_units = p->num_tiles * splits;
+    q.split_rows = p->tiles_m * block_M;
     q.bm = block_M;
     q.bn = block_N;
     q.bk = block_K;
@@ -760,7 +841,8 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     q.m_halves = L.m_halves;
     q.a_rows = L.a_rows;
     q.b_rows = L.b_rows;
-    q.out_mode = out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
+    // The kernel's own output: fp32 partials when K is split, else C's type.
+    q.out_mode = splits > 1 ? 0 : out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
     q.acc_stages = L.acc_stages;
     q.acc_cols = L.acc_cols;
     q.tmem_cols = L.tmem_cols;
@@ -811,10 +893,17 @@ static int prepare_maps(tgemm_plan_s *p, const void *A, const void *B, void *C)
             rc = encode_2d(&q.tmB, p->dtype, B, uint64_t(p->K), uint64_t(p->N), uint64_t(p->K) * L.in_bytes,
                            uint32_t(L.bk), uint32_t(L.b_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
-    if (rc == kOk)
-        rc = encode_2d(&q.tmC, p->out_dtype, C, uint64_t(p->N), uint64_t(p->M), uint64_t(p->N) * L.out_bytes,
-                       uint32_t(kEpiCols), 32u, L.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                       CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (rc == kOk) {
+        if (p->splits > 1)  // partial tiles go to the workspace, viewed as [splits * M, N] fp32
+            rc = encode_2d(&q.tmC, kF32, p->d_work, uint64_t(p->N), uint64_t(p->splits) * uint64_t(q.split_rows),
+                           uint64_t(p->N) * 4u, uint32_t(kEpiCols), 32u, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE);
+        else
+            rc = encode_2d(&q.tmC, p->out_dtype, C, uint64_t(p->N), uint64_t(p->M), uint64_t(p->N) * L.out_bytes,
+                           uint32_t(kEpiCols), 32u,
+                           L.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    }
     if (rc != kOk) {
         p->maps_valid = false;
         return rc;
@@ -853,10 +942,22 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
             cudaGetLastError();
             return kErrCuda;
         }
-        return kOk;
+    } else {
+        tgemm_kernel<false><<<p->grid, kThreads, p->smem_launch, reinterpret_cast<cudaStream_t>(stream)>>>(p->params);
+        if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     }
-    tgemm_kernel<false><<<p->grid, kThreads, p->smem_launch, reinterpret_cast<cudaStream_t>(stream)>>>(p->params);
-    if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+    if (p->splits > 1) {
+        const int64_t mn = p->M * p->N;
+        const int64_t n4 = mn / 4;
+        int blocks = int((n4 + 255) / 256);
+        const int cap = 8 * p->num_sms;
+        if (blocks > cap) blocks = cap;
+        const int out_mode = p->out_dtype == kF32 ? 0 : p->out_dtype == kF16 ? 1 : 2;
+        const int64_t stride = int64_t(p->params.split_rows) * p->N;
+        splitk_reduce_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p->d_work, C, mn, stride,
+                                                                                         p->splits, out_mode);
+        if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+    }
     return kOk;
 }
 
@@ -938,6 +1039,8 @@ int tgemm_get_plan_info(tgemm_plan_t p, tgemm_plan_info *info)
     info->smem_limit = p->smem_limit;
     info->num_sms = p->num_sms;
     info->cta_pair = p->pair;
+    info->split_k = p->splits;
+    info->num_units = p->params.num_units;
     return kOk;
 }
 
@@ -946,6 +1049,10 @@ int tgemm_destroy(tgemm_plan_t p)
     if (!p) return kOk;
     int rc = kOk;
     if (p->d_status && cudaFree(p->d_status) != cudaSuccess) {
+        cudaGetLastError();
+        rc = kErrCuda;
+    }
+    if (p->d_work && cudaFree(p->d_work) != cudaSuccess) {
         cudaGetLastError();
         rc = kErrCuda;
     }
@@ -1054,6 +1161,10 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     q.tiles_m = tiles_m;
     q.tiles_n = tiles_n;
     q.num_tiles = tiles;
+    q.splits = 1;
+    q.kb_per_split = q.num_kb;
+    q.num_units = tiles;
+    q.split_rows = tiles_m * block_M;
     q.group_m = 8;
     q.bm = block_M;
     q.bn = block_N;

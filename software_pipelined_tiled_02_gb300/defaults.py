@@ -12,12 +12,13 @@ pages say of cost models; the sweep decides.
 
 from __future__ import annotations
 
-# (M, N, K, operand dtype, out dtype) -> (block, num_stages); dtype codes 0 f16, 1 bf16, 2 f32.
+# (M, N, K, operand dtype, out dtype) -> (block, num_stages[, cta_pair[, split_k]]);
+# dtype codes 0 f16, 1 bf16, 2 f32.
 FROZEN = {
     (4096, 4096, 4096, 0, 0): ((256, 224, 64), 3),      # 1584 TFLOP/s
     (8192, 8192, 8192, 1, 1): ((256, 256, 64), 3),      # 1849 TFLOP/s
     (4000, 3000, 5000, 0, 2): ((256, 192, 64), 3),      # 988 TFLOP/s
-    (512, 512, 32768, 0, 2): ((128, 64, 64), 4),        # 107 TFLOP/s (32 tiles: SM coverage bound)
+    (512, 512, 32768, 0, 2): ((128, 128, 64), 6, False, 9),  # 484 TFLOP/s; 107 unsplit (16 tiles for 152 SMs)
     (128, 128, 128, 0, 2): ((128, 128, 32), 3),
 }
 
@@ -45,10 +46,11 @@ def estimate(M: int, N: int, K: int, block, rel: float, num_sms: int = DEFAULT_S
     return waves * bm * bn * max(K, 1) / rel
 
 
-def choose(M: int, N: int, K: int, dtype: int, out_dtype: int, num_sms: int = DEFAULT_SMS):
-    """(block, num_stages, cta_pair) for a problem."""
+def choose(M: int, N: int, K: int, dtype: int, out_dtype: int, num_sms: int = DEFAULT_SMS) -> dict:
+    """{block, num_stages, cta_pair, split_k} for a problem."""
     hit = FROZEN.get((M, N, K, dtype, out_dtype))
     if hit is not None:
-        return hit[0], hit[1], (hit[2] if len(hit) > 2 else False)
+        return {"block": hit[0], "num_stages": hit[1], "cta_pair": hit[2] if len(hit) > 2 else False,
+                "split_k": hit[3] if len(hit) > 3 else 1}
     best = min(CANDIDATES, key=lambda c: (estimate(M, N, K, c[0], c[2], num_sms), -c[2]))
-    return best[0], best[1], False
+    return {"block": best[0], "num_stages": best[1], "cta_pair": False, "split_k": 1}

@@ -24,10 +24,10 @@ def to_dev(bits, dtype):
     return inputs.bits_to_torch(bits, dtype).cuda()
 
 
-def run(tg, A, B, dtype, out, block, stages, pair=False):
+def run(tg, A, B, dtype, out, block, stages, pair=False, split_k=1):
     M, K = A.shape
     N = B.shape[0]
-    plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair)
+    plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair, split_k=split_k)
     dA, dB = to_dev(A, dtype), to_dev(B, dtype)
     C = torch.full((M, N), float("nan"), dtype=TORCH[out], device="cuda")
     plan.run(dA, dB, C)
@@ -148,6 +148,46 @@ def test_pair_full_size_sampled(cuda_lib, name, block, stages):
     assert_close(as_f64(got), R, S, w["out"])
 
 
+# ------------------------------------------------------------ split-K
+
+SPLIT_CONFIGS = [((128, 128, 64), 4, 4, False), ((128, 64, 32), 3, 7, False), ((256, 128, 64), 3, 3, False),
+                 ((256, 256, 64), 4, 2, True), ((128, 32, 16), 2, 64, False)]
+
+
+@pytest.mark.parametrize("block,stages,splits,pair", SPLIT_CONFIGS, ids=lambda v: str(v))
+@pytest.mark.parametrize("shape", [(300, 200, 1032), (520, 264, 4096), (64, 32, 8), (257, 96, 200)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("bf16", "bf16"), ("f16", "f16")])
+def test_split_k_parity(cuda_lib, block, stages, splits, pair, shape, dtype, out):
+    M, N, K = shape
+    A, B = inputs.operands(300 + M + K, M, N, K, dtype, "uniform")
+    C = as_f64(run(cuda_lib, A, B, dtype, out, block, stages, pair, splits))
+    R, S = oracle.gemm(A, B, dtype)
+    assert_close(C, R, S, out)
+
+
+def test_split_k_integer_exact_and_stage_invariant(cuda_lib):
+    M, N, K = 512, 512, 8192
+    A, B = inputs.operands(43, M, N, K, "f16", "int", lo=-4, hi=4)
+    R, _ = oracle.gemm(A, B, "f16")
+    outs = [run(cuda_lib, A, B, "f16", "f32", (128, 128, 64), s, split_k=8) for s in (1, 2, 4, 6)]
+    assert np.array_equal(as_f64(outs[0]), R)
+    for C in outs[1:]:
+        assert torch.equal(C.view(torch.int32), outs[0].view(torch.int32))
+
+
+def test_split_k_plan_reports_effective_splits(cuda_lib):
+    # 3 k-blocks cannot be cut 8 ways: one k-block per split at most.
+    plan = cuda_lib.Plan(256, 256, 192, "f16", "f32", (128, 128, 64), 2, split_k=8)
+    assert plan.info["split_k"] == 3 and plan.info["num_units"] == 4 * 3
+    plan.close()
+    plan = cuda_lib.Plan(256, 256, 64, "f16", "f32", (128, 128, 64), 2, split_k=8)
+    assert plan.info["split_k"] == 1
+    plan.close()
+    rc, h = cuda_lib.tgemm_plan_ex(256, 256, 256, "f16", "f32", 128, 128, 64, 2, split_k=65)
+    assert rc == cuda_lib.ERR_INVALID_ARG and h is None
+
+
 # ------------------------------------------------------------ degenerate cases
 
 def test_empty_product_is_a_noop(cuda_lib):
@@ -253,12 +293,13 @@ def sample_entries(M, N, n_random, seed):
     return np.concatenate(rows), np.concatenate(cols)
 
 
-def full_size(cuda_lib, name, block=None, stages=None, pair=False):
+def full_size(cuda_lib, name, block=None, stages=None, pair=False, split_k=1):
     w = inputs.WORKLOADS[name]
     A, B = inputs.workload_operands(name)
     if block is None:
-        block, stages, pair = cuda_lib.default_config(w["M"], w["N"], w["K"], w["dtype"], w["out"])
-    C = run(cuda_lib, A, B, w["dtype"], w["out"], block, stages, pair)
+        cfg = cuda_lib.default_config(w["M"], w["N"], w["K"], w["dtype"], w["out"])
+        block, stages, pair, split_k = cfg["block"], cfg["num_stages"], cfg["cta_pair"], cfg["split_k"]
+    C = run(cuda_lib, A, B, w["dtype"], w["out"], block, stages, pair, split_k)
     return w, A, B, C
 
 
