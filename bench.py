@@ -385,7 +385,8 @@ def run_ours(args, w, world, rank, local):
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": recorded_traffic(args.workload),
                 "peak_source": f"{peak_src} dense bf16 burst (fp16 runs at the bf16 rate: nominal ratio 1)",
-                "kernel": "tgemm_kernel", "flops_per_launch": flops,
+                "kernel": ("tgemm_kernel + splitk_reduce_kernel, timed together per step" if info["split_k"] > 1
+                           else "tgemm_kernel"), "flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": (M * K + N * K) * 2 + M * N * (4 if w["out"] == "f32" else 2)}
 
     line = None
