@@ -139,11 +139,20 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
  *     The order of every sum depends only on the tile shape and s, never on
  *     num_stages, so results stay bit-identical across depths.  For long K
  *     and few output tiles (more SMs than tiles).  At most 64.
+ *   prefetch: 0 = num_stages.  1 <= D <= num_stages = the producer issues the
+ *     loads of k-block i only after the MMAs of k-block i - D have finished,
+ *     i.e. it runs at most D k-blocks ahead whatever the number of buffers.
+ *     This separates the pipeline depth from the buffer count the way the
+ *     pages separate a manual schedule's max(stage) + 1 from num_stages
+ *     (chapter 11 sections 3.3 and 4.4): D = 1 serialises load and compute,
+ *     D = 2 is the two-stage schedule of matmul_manual.  Results do not
+ *     depend on D.
  */
 typedef struct tgemm_plan_opts {
     int cta_pair;
     int group_m;
     int split_k;
+    int prefetch;
 } tgemm_plan_opts;
 
 /* tgemm_validate with options (NULL = defaults). */
@@ -218,6 +227,7 @@ typedef struct tgemm_plan_info {
     int cta_pair;        /* 1: clusters of two CTAs share each tile */
     int split_k;         /* effective K splits (1: none) */
     int num_units;       /* persistent work units: tiles x K splits */
+    int prefetch;        /* producer lead in k-blocks */
 } tgemm_plan_info;
 
 int tgemm_get_plan_info(tgemm_plan_t plan, tgemm_plan_info *info);

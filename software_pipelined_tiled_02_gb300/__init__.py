@@ -45,14 +45,16 @@ class PlanInfo(ctypes.Structure):
                 ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("num_k_blocks", ctypes.c_int),
                 ("acc_stages", ctypes.c_int), ("tmem_columns", ctypes.c_int), ("smem_bytes", ctypes.c_int64),
                 ("smem_bound", ctypes.c_int64), ("smem_limit", ctypes.c_int), ("num_sms", ctypes.c_int),
-                ("cta_pair", ctypes.c_int), ("split_k", ctypes.c_int), ("num_units", ctypes.c_int)]
+                ("cta_pair", ctypes.c_int), ("split_k", ctypes.c_int), ("num_units", ctypes.c_int),
+                ("prefetch", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class PlanOpts(ctypes.Structure):
-    _fields_ = [("cta_pair", ctypes.c_int), ("group_m", ctypes.c_int), ("split_k", ctypes.c_int)]
+    _fields_ = [("cta_pair", ctypes.c_int), ("group_m", ctypes.c_int), ("split_k", ctypes.c_int),
+                ("prefetch", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -152,18 +154,18 @@ def tgemm_plan(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages)
 
 
 def tgemm_plan_ex(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, cta_pair=0, group_m=0,
-                  split_k=0):
+                  split_k=0, prefetch=0):
     """Returns ``(status, handle)``; handle is None on failure."""
     h = ctypes.c_void_p()
-    opts = PlanOpts(int(cta_pair), int(group_m), int(split_k))
+    opts = PlanOpts(int(cta_pair), int(group_m), int(split_k), int(prefetch))
     rc = load().tgemm_plan_ex(ctypes.byref(h), M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K,
                               num_stages, ctypes.byref(opts))
     return int(rc), (h if rc == OK else None)
 
 
 def tgemm_validate_ex(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit, cta_pair=0,
-                      group_m=0, split_k=0) -> int:
-    opts = PlanOpts(int(cta_pair), int(group_m), int(split_k))
+                      group_m=0, split_k=0, prefetch=0) -> int:
+    opts = PlanOpts(int(cta_pair), int(group_m), int(split_k), int(prefetch))
     return int(load().tgemm_validate_ex(M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K,
                                         num_stages, smem_limit, ctypes.byref(opts)))
 
@@ -227,13 +229,13 @@ class Plan:
     """A validated GEMM configuration on the current CUDA device."""
 
     def __init__(self, M, N, K, dtype="f16", out_dtype=None, block=(128, 256, 64), num_stages=4, pair=False,
-                 split_k=1):
+                 split_k=1, prefetch=0):
         dtype = _dt(dtype)
         out_dtype = dtype if out_dtype is None else _dt(out_dtype)
         bm, bn, bk = block
-        if pair or split_k > 1:
+        if pair or split_k > 1 or prefetch:
             rc, h = tgemm_plan_ex(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages, cta_pair=int(bool(pair)),
-                                  split_k=int(split_k))
+                                  split_k=int(split_k), prefetch=int(prefetch))
         else:
             rc, h = tgemm_plan(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages)
         if rc != OK:

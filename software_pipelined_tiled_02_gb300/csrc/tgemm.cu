@@ -60,6 +60,7 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     int num_kb;                 // ceil(K / bk)
     int tiles_m, tiles_n, num_tiles, group_m;
     int splits, kb_per_split;   // K splits per tile (1: none) and k-blocks per split
+    int prefetch;               // producer lead in k-blocks, 1..stages (stages: the full ring)
     int split_rows;             // workspace rows per split: tiles_m * block_M, so a tile's
                                 // ragged tail stays inside its own split's rows
     int num_units;              // work units: num_tiles * splits
@@ -356,6 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         uint32_t ph = 0;
         int issued = 0;
         bool ok = true;
+        // Prefetch distance D < S: before loading k-block i, also wait until
+        // the MMAs of k-block i - D have released their slot (slot (i-D) % S,
+        // whose latest use is i - D because (i - D) + S > i).
+        const int D = p.prefetch;
+        int sd = S - D;  // slot of iteration issued - D, once issued >= D
+        uint32_t phd = 0;
         for (int t = unit0; ok && t < p.num_units; t += ustride) {
             const Unit w = unit_coords(p, t);
             const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn + int(rank) * p.b_rows;
@@ -363,6 +370,16 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                 if (!warp_wait(empty(s), ph ^ 1u, p, abort, 0, issued)) {
                     ok = false;
                     break;
+                }
+                if (D < S) {
+                    if (issued >= D && !warp_wait(empty(sd), phd, p, abort, 0, issued)) {
+                        ok = false;
+                        break;
+                    }
+                    if (++sd == S) {
+                        sd = 0;
+                        if (issued >= D) phd ^= 1u;
+                    }
                 }
                 if (lane == 0) {
                     if constexpr (PAIR) {
@@ -726,6 +743,7 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     if (opts && (opts->cta_pair != 0 && opts->cta_pair != 1)) return kErrInvalidArg;
     if (opts && (opts->group_m < 0 || opts->group_m > 4096)) return kErrInvalidArg;
     if (opts && (opts->split_k < 0 || opts->split_k > kMaxSplits)) return kErrInvalidArg;
+    if (opts && (opts->prefetch < 0 || opts->prefetch > num_stages)) return kErrInvalidArg;
     const int splits = effective_splits(K, block_K, opts && opts->split_k > 1 ? opts->split_k : 1);
     // Argument checks that need no device come first.
     int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX, pair, splits);
@@ -831,6 +849,7 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     q.splits = splits;
     // effective_splits guarantees every split a non-empty k-block range
     q.kb_per_split = splits > 1 ? (q.num_kb + splits - 1) / splits : q.num_kb;
+    q.prefetch = opts && opts->prefetch > 0 ? opts->prefetch : num_stages;
     q.num_units = p->num_tiles * splits;
     q.split_rows = p->tiles_m * block_M;
     q.bm = block_M;
@@ -1040,6 +1059,7 @@ int tgemm_get_plan_info(tgemm_plan_t p, tgemm_plan_info *info)
     info->num_sms = p->num_sms;
     info->cta_pair = p->pair;
     info->split_k = p->splits;
+    info->prefetch = p->params.prefetch;
     info->num_units = p->params.num_units;
     return kOk;
 }
@@ -1163,6 +1183,7 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     q.num_tiles = tiles;
     q.splits = 1;
     q.kb_per_split = q.num_kb;
+    q.prefetch = num_stages;
     q.num_units = tiles;
     q.split_rows = tiles_m * block_M;
     q.group_m = 8;

@@ -135,7 +135,8 @@ class Runner:
         row = dict(c)
         try:
             plan = tg.Plan(self.M, self.N, self.K, w["dtype"], w["out"],
-                           (c["block_M"], c["block_N"], c["block_K"]), c["num_stages"], pair=bool(c.get("cta_pair")))
+                           (c["block_M"], c["block_N"], c["block_K"]), c["num_stages"], pair=bool(c.get("cta_pair")),
+                           prefetch=int(c.get("prefetch", 0)))
         except tg.TgemmError as e:
             row.update(ok=False, error=str(e))
             return row
@@ -170,6 +171,8 @@ def main(argv=None):
     ap.add_argument("--space", choices=("pages", "gb300"), default="gb300")
     ap.add_argument("--any-tile", action="store_true", help="keep tiles that do not divide the problem")
     ap.add_argument("--stage-curve", action="store_true", help="latency and smem vs num_stages for 3 tile shapes")
+    ap.add_argument("--prefetch-curve", action="store_true",
+                    help="latency vs the producer's prefetch distance at a fixed number of buffers")
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--out", default=None, help="write all rows as JSON here")
     ap.add_argument("--no-cache", action="store_true", help="do not write the per-device best config")
@@ -185,7 +188,19 @@ def main(argv=None):
     runner = Runner(args.workload, reps=args.reps)
     report = {"workload": args.workload, "device": dev, "smem_limit": limit}
 
-    if args.stage_curve:
+    if args.prefetch_curve:
+        curve = []
+        for block, S in (((128, 128, 32), 6), ((128, 256, 64), 4)):
+            for D in range(1, S + 1):
+                c = dict(block_M=block[0], block_N=block[1], block_K=block[2], num_stages=S, prefetch=D)
+                curve.append(runner.run(c))
+        report["prefetch_curve"] = curve
+        print("| tile | buffers (num_stages) | prefetch distance | median µs | TFLOP/s | parity |")
+        print("|---|---|---|---|---|---|")
+        for r in curve:
+            print(f"| {r['block_M']}x{r['block_N']}x{r['block_K']} | {r['num_stages']} | {r['prefetch']} | "
+                  f"{1e3 * r['median_ms']:.1f} | {r['tflops']:.0f} | {'ok' if r['ok'] else 'FAIL'} |")
+    elif args.stage_curve:
         curve = []
         for block in ((128, 128, 32), (128, 256, 64), (256, 256, 64)):
             for S in (1, 2, 3, 4, 6, 8):

@@ -59,3 +59,25 @@ def test_bit_identical_across_stages_pair(cuda_lib, block, stage_list):
     res = outputs_over_stages(cuda_lib, 1000, 1040, 2056, "bf16", "f32", block, stage_list, seed=78, pair=True)
     for s, C in zip(stage_list[1:], res[1:]):
         assert torch.equal(bits(C), bits(res[0])), f"num_stages={s} differs"
+
+
+def test_bit_identical_across_prefetch_distances(cuda_lib):
+    # The producer's lead D (1 = serial copy/compute, 2 = the two-stage manual
+    # schedule, ... S = the full ring) changes timing only.
+    M, N, K = 1000, 1040, 2056
+    A, B = inputs.operands(79, M, N, K, "f16", "normal")
+    dA = inputs.bits_to_torch(A, "f16").cuda()
+    dB = inputs.bits_to_torch(B, "f16").cuda()
+    res = []
+    for D in (1, 2, 3, 5, 6):
+        plan = cuda_lib.Plan(M, N, K, "f16", "f32", (128, 128, 32), 6, prefetch=D)
+        assert plan.info["prefetch"] == D
+        C = plan.run(dA, dB)
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+        res.append(C)
+        plan.close()
+    for C in res[1:]:
+        assert torch.equal(bits(C), bits(res[0]))
+    rc, h = cuda_lib.tgemm_plan_ex(M, N, K, "f16", "f32", 128, 128, 32, 4, prefetch=5)
+    assert rc == cuda_lib.ERR_INVALID_ARG and h is None
