@@ -324,3 +324,46 @@ def test_long_k_integer_exact(cuda_lib):
     w, A, B, C = full_size(cuda_lib, "gemm_512x512x32768_f16_int")
     R, _ = oracle.gemm(A, B, w["dtype"])
     assert np.array_equal(as_f64(C), R)
+
+
+# ------------------------------------------------------------ large coordinates
+
+@pytest.mark.parametrize("M,N,K,block,stages,split,nrand", [
+    (1 << 20, 64, 64, (128, 64, 64), 4, 1, 4096),      # a million rows: tile row coordinates up to 2^20
+    (128, 96, 1 << 19, (128, 96, 64), 6, 16, 128),     # a half-million-deep reduction, split 16 ways
+    (96, 1 << 18, 128, (128, 256, 64), 4, 1, 4096),    # a quarter-million columns
+])
+def test_large_coordinates_sampled(cuda_lib, M, N, K, block, stages, split, nrand):
+    A, B = inputs.operands(51, M, N, K, "bf16", "uniform")
+    C = run(cuda_lib, A, B, "bf16", "f32", block, stages, split_k=split)
+    rows, cols = sample_entries(M, N, nrand, 9)
+    if M * N > 1 << 20:  # whole first/last rows and columns of a huge C: keep a strided subset
+        keep = np.arange(rows.size) % 8 == 0
+        rows, cols = rows[keep], cols[keep]
+    R, S = oracle.gemm_entries(A, B, "bf16", rows, cols)
+    got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+    assert_close(as_f64(got), R, S, "f32")
+
+
+def test_gemm_convenience_api_uses_tuned_defaults(cuda_lib):
+    M, N, K = 512, 512, 32768
+    A, B = inputs.operands(52, M, N, K, "f16", "uniform")
+    dA, dB = to_dev(A, "f16"), to_dev(B, "f16")
+    C = cuda_lib.gemm(dA, dB, out_dtype=torch.float32)  # frozen default: split-K
+    C2 = cuda_lib.gemm(dA, dB, out_dtype=torch.float32)  # cached plan
+    torch.cuda.synchronize()
+    R, S = oracle.gemm(A, B, "f16")
+    assert_close(as_f64(C), R, S, "f32")
+    assert torch.equal(C, C2)
+    with pytest.raises(cuda_lib.TgemmError):
+        cuda_lib.gemm(dA.float(), dB.float())
+    with pytest.raises(ValueError):
+        cuda_lib.gemm(dA, dB[:, :-8])
+
+
+def test_run_host_argument_errors(cuda_lib):
+    plan = cuda_lib.Plan(128, 128, 64, "f16", "f32", (128, 128, 32), 3)
+    x = torch.zeros(128 * 128, dtype=torch.float32, device="cuda").data_ptr()
+    assert cuda_lib.tgemm_run_host(plan.handle, 0, 0, 0, x, x, x) == cuda_lib.ERR_INVALID_ARG
+    assert cuda_lib.tgemm_run_host(None, 0, 0, 0, 0, 0, 0) == cuda_lib.ERR_INVALID_ARG
+    plan.close()
