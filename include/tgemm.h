@@ -95,8 +95,9 @@ int tgemm_smem_limit(void);
  *   - M, N >= 0, K >= 0, each < 2^31; num_stages >= 1      -> INVALID_ARG
  *   - K % 8 == 0, N * out_bytes % 16 == 0 (row pitch)      -> ALIGNMENT
  *   - block_M in {128, 256}; block_N a multiple of 32 in
- *     [32, 256]; block_K in {16, 32, 64} (16-bit operands:
- *     rows of 32, 64 or 128 bytes)                          -> NO_KERNEL
+ *     [32, 256]; block_K in {16, 32, 64, 128} (16-bit
+ *     operands: rows of 32, 64 or 128 bytes, or two 128-byte
+ *     K-panels for 128)                                     -> NO_KERNEL
  *   - tgemm_smem_bound > smem_limit or
  *     tgemm_smem_bytes > smem_limit                         -> SMEM_BUDGET
  * The budget rule is the one of chapter 11 sections 4.5 and 5.1: a config

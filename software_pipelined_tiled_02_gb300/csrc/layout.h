@@ -47,23 +47,26 @@ struct Layout {
     int acc_cols;            // TMEM columns of one accumulator (m_halves * bn)
     int acc_stages;          // accumulators in flight (2 lets the epilogue overlap the next tile)
     int tmem_cols;           // power of two >= 32 allocated per CTA
-    int swizzle_bytes;       // operand row bytes = bk * in_bytes: 32, 64 or 128
+    int swizzle_bytes;       // bytes of one operand row within a K-panel: 32, 64 or 128
+    int panels;              // K-panels per slot: 1, or 2 when a row is 256 bytes
 };
 
 inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 // Tile shapes the kernel implements: M = 128 MMAs (one or two per k-step),
 // N a multiple of 32 up to the MMA maximum of 256, and block_K such that a
-// K-contiguous operand row is exactly one swizzle span (32, 64 or 128 bytes).
-// The CTA-pair mode implements only block_M = 256 (one M = 256 MMA over the
-// two CTAs' 128-row halves).
+// K-contiguous operand row is one swizzle span (32, 64 or 128 bytes) or two
+// 128-byte spans (block_K = 128 for 16-bit operands: the slot then holds two
+// K-panels of 64 elements, each a standard 128-byte-swizzled tile).  The
+// CTA-pair mode implements only block_M = 256 (one M = 256 MMA over the two
+// CTAs' 128-row halves).
 inline bool tile_supported(int bm, int bn, int bk, int in_bytes, int pair = 0)
 {
     if (pair && bm != 256) return false;
     if (bm != 128 && bm != 256) return false;
     if (bn < 32 || bn > 256 || bn % 32 != 0) return false;
     int row = bk * in_bytes;
-    return (row == 32 || row == 64 || row == 128) && bk > 0;
+    return (row == 32 || row == 64 || row == 128 || row == 256) && bk > 0;
 }
 
 // Barrier block: full[S], empty[S], acc_full[2], acc_empty[2], drain, stall
@@ -101,7 +104,8 @@ inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out
     int cols = 32;
     while (cols < need) cols <<= 1;
     L.tmem_cols = cols;
-    L.swizzle_bytes = bk * L.in_bytes;
+    L.swizzle_bytes = bk * L.in_bytes > 128 ? 128 : bk * L.in_bytes;
+    L.panels = bk * L.in_bytes / L.swizzle_bytes;
     return L;
 }
 

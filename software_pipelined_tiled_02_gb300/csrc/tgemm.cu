@@ -73,7 +73,9 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     uint32_t idesc;             // tcgen05 instruction descriptor (kind::f16)
     uint32_t a_slot, b_slot;    // bytes between consecutive ring slots
     uint32_t stage_tx;          // bytes the TMA delivers per slot (A box + B box)
-    uint32_t row_bytes;         // bytes of one K-contiguous operand row in a slot
+    uint32_t row_bytes;         // bytes of one operand row within a K-panel (the swizzle span)
+    int panels, panel_k;        // K-panels per slot (1 or 2) and elements per panel
+    uint32_t a_panel16, b_panel16;  // distance between a slot's K-panels, in 16-byte units
     uint32_t off_a, off_b, off_c, off_bar, c_buf_bytes;
     int epi_bufs;               // staging buffers per epilogue warp (1 or 2)
     uint32_t desc_lo_flags;     // leading-byte-offset field of the smem descriptor
@@ -204,6 +206,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
     const uint64_t ad0 = smem_desc(c.sA, p), bd0 = smem_desc(c.sB, p);
     const uint64_t a_step = p.a_slot >> 4, b_step = p.b_slot >> 4;
     const uint64_t a_half = (128u * p.row_bytes) >> 4;
+    const uint64_t a_panel = p.a_panel16, b_panel = p.b_panel16;
     int s = 0;
     uint32_t ph = 0;
     uint64_t ad = ad0, bd = bd0;
@@ -229,10 +232,12 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
                 const uint32_t first = kb != kb0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < NK; ++kk) {
+                    // k-step kk: 32-byte step (kk % 4) inside K-panel kk / 4
+                    const uint64_t ka = uint64_t(2 * (kk & 3)) + uint64_t(kk >> 2) * a_panel;
+                    const uint64_t kb_ = uint64_t(2 * (kk & 3)) + uint64_t(kk >> 2) * b_panel;
 #pragma unroll
                     for (int h = 0; h < MH; ++h)
-                        mma(h ? d2 : d, ad + uint64_t(2 * kk) + (h ? a_half : 0), bd + uint64_t(2 * kk),
-                            kk == 0 ? first : 1u);
+                        mma(h ? d2 : d, ad + ka + (h ? a_half : 0), bd + kb_, kk == 0 ? first : 1u);
                 }
                 commit_both(empty(s));  // slot s (in both CTAs) may be refilled once these MMAs finish
             }
@@ -273,7 +278,8 @@ __device__ __forceinline__ void mma_dispatch_nk(const Params &p, const MmaCtx &c
     switch (p.n_kstep) {
     case 1: mma_role<1, MH, PAIR>(p, c, abort, lane); break;
     case 2: mma_role<2, MH, PAIR>(p, c, abort, lane); break;
-    default: mma_role<4, MH, PAIR>(p, c, abort, lane); break;
+    case 4: mma_role<4, MH, PAIR>(p, c, abort, lane); break;
+    default: mma_role<8, MH, PAIR>(p, c, abort, lane); break;
     }
 }
 
@@ -382,15 +388,22 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                     }
                 }
                 if (lane == 0) {
+                    const uint32_t a_dst = sA + uint32_t(s) * p.a_slot, b_dst = sB + uint32_t(s) * p.b_slot;
                     if constexpr (PAIR) {
                         const uint32_t fb = full_leader + 8u * uint32_t(s);
                         if (rank == 0) mbar_arrive_expect_tx(full(s), p.stage_tx);
-                        tma_load_2d_pair(sA + uint32_t(s) * p.a_slot, &p.tmA, kb * p.bk, m0, fb);
-                        tma_load_2d_pair(sB + uint32_t(s) * p.b_slot, &p.tmB, kb * p.bk, n0, fb);
+                        for (int pl = 0; pl < p.panels; ++pl) {
+                            const int x = kb * p.bk + pl * p.panel_k;
+                            tma_load_2d_pair(a_dst + (uint32_t(pl) * p.a_panel16 << 4), &p.tmA, x, m0, fb);
+                            tma_load_2d_pair(b_dst + (uint32_t(pl) * p.b_panel16 << 4), &p.tmB, x, n0, fb);
+                        }
                     } else {
                         mbar_arrive_expect_tx(full(s), p.stage_tx);
-                        tma_load_2d(sA + uint32_t(s) * p.a_slot, &p.tmA, kb * p.bk, m0, full(s));
-                        tma_load_2d(sB + uint32_t(s) * p.b_slot, &p.tmB, kb * p.bk, n0, full(s));
+                        for (int pl = 0; pl < p.panels; ++pl) {
+                            const int x = kb * p.bk + pl * p.panel_k;
+                            tma_load_2d(a_dst + (uint32_t(pl) * p.a_panel16 << 4), &p.tmA, x, m0, full(s));
+                            tma_load_2d(b_dst + (uint32_t(pl) * p.b_panel16 << 4), &p.tmB, x, n0, full(s));
+                        }
                     }
                 }
                 __syncwarp();
@@ -877,6 +890,10 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     // Bytes that complete one full[s] phase: this CTA's boxes, or both CTAs' in pair mode.
     q.stage_tx = (L.a_stage_bytes + L.b_stage_bytes) * (pair ? 2u : 1u);
     q.row_bytes = uint32_t(L.swizzle_bytes);
+    q.panels = L.panels;
+    q.panel_k = L.swizzle_bytes / L.in_bytes;
+    q.a_panel16 = (uint32_t(L.a_rows) * uint32_t(L.swizzle_bytes)) >> 4;
+    q.b_panel16 = (uint32_t(L.b_rows) * uint32_t(L.swizzle_bytes)) >> 4;
     q.off_a = L.off_a;
     q.off_b = L.off_b;
     q.off_c = L.off_c;
@@ -906,11 +923,12 @@ static int prepare_maps(tgemm_plan_s *p, const void *A, const void *B, void *C)
     int rc = kOk;
     if (p->K > 0) {
         CUtensorMapSwizzle swz = swizzle_for(L.swizzle_bytes);
-        rc = encode_2d(&q.tmA, p->dtype, A, uint64_t(p->K), uint64_t(p->M), uint64_t(p->K) * L.in_bytes,
-                       uint32_t(L.bk), uint32_t(L.a_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        const uint32_t box_k = uint32_t(L.swizzle_bytes / L.in_bytes);  // one K-panel per box
+        rc = encode_2d(&q.tmA, p->dtype, A, uint64_t(p->K), uint64_t(p->M), uint64_t(p->K) * L.in_bytes, box_k,
+                       uint32_t(L.a_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (rc == kOk)
-            rc = encode_2d(&q.tmB, p->dtype, B, uint64_t(p->K), uint64_t(p->N), uint64_t(p->K) * L.in_bytes,
-                           uint32_t(L.bk), uint32_t(L.b_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+            rc = encode_2d(&q.tmB, p->dtype, B, uint64_t(p->K), uint64_t(p->N), uint64_t(p->K) * L.in_bytes, box_k,
+                           uint32_t(L.b_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
     if (rc == kOk) {
         if (p->splits > 1)  // partial tiles go to the workspace, viewed as [splits * M, N] fp32
@@ -1088,7 +1106,9 @@ const char *tgemm_strerror(int code)
     case kErrUnsupportedDtype: return "unsupported dtype (operands fp16/bf16; output fp32 or the operand dtype)";
     case kErrAlignment: return "pointer or row pitch not a multiple of 16 bytes";
     case kErrSmemBudget: return "num_stages x (A tile + B tile) exceeds the per-block shared-memory limit";
-    case kErrNoKernel: return "tile shape not implemented (block_M 128/256, block_N 32..256 step 32, block_K 16/32/64)";
+    case kErrNoKernel:
+        return "tile shape not implemented (block_M 128/256, block_N 32..256 step 32, block_K 16/32/64/128; "
+               "CTA pairs need block_M 256)";
     case kErrArch: return "device is not compute capability 10.3 (GB300)";
     case kErrCuda: return "CUDA runtime or driver call failed";
     case kErrTimeout: return "a pipeline wait in the kernel exceeded the watchdog limit";
@@ -1205,6 +1225,10 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     q.b_slot = round_up(L.b_stage_bytes, kSmemAlign);
     q.stage_tx = L.a_stage_bytes + L.b_stage_bytes;
     q.row_bytes = uint32_t(L.swizzle_bytes);
+    q.panels = L.panels;
+    q.panel_k = L.swizzle_bytes / L.in_bytes;
+    q.a_panel16 = (uint32_t(L.a_rows) * uint32_t(L.swizzle_bytes)) >> 4;
+    q.b_panel16 = (uint32_t(L.b_rows) * uint32_t(L.swizzle_bytes)) >> 4;
     q.off_a = L.off_a;
     q.off_b = L.off_b;
     q.off_c = L.off_c;
@@ -1219,10 +1243,11 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     q.debug_stall = 0;
     if (K > 0) {
         const CUtensorMapSwizzle swz = swizzle_for(L.swizzle_bytes);
-        rc = encode_2d(&q.tmA, dtype, A, uint64_t(K), uint64_t(M), uint64_t(K) * L.in_bytes, uint32_t(L.bk),
+        const uint32_t box_k = uint32_t(L.swizzle_bytes / L.in_bytes);  // one K-panel per box
+        rc = encode_2d(&q.tmA, dtype, A, uint64_t(K), uint64_t(M), uint64_t(K) * L.in_bytes, box_k,
                        uint32_t(L.a_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (rc == kOk)
-            rc = encode_2d(&q.tmB, dtype, B, uint64_t(K), uint64_t(N), uint64_t(K) * L.in_bytes, uint32_t(L.bk),
+            rc = encode_2d(&q.tmB, dtype, B, uint64_t(K), uint64_t(N), uint64_t(K) * L.in_bytes, box_k,
                            uint32_t(L.b_rows), swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
     if (rc == kOk)

@@ -106,7 +106,8 @@ def test_validate_rules(lib):
     assert V(128, 128, 128, tg.F16, tg.F32, 64, 128, 32, 3, L) == tg.ERR_NO_KERNEL
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 48, 32, 3, L) == tg.ERR_NO_KERNEL
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 512, 32, 3, L) == tg.ERR_NO_KERNEL
-    assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 128, 1, L) == tg.ERR_NO_KERNEL
+    assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 128, 1, L) == tg.OK  # two 64-wide K-panels per slot
+    assert V(128, 128, 256, tg.F16, tg.F32, 128, 128, 256, 1, L) == tg.ERR_NO_KERNEL
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 8, 3, L) == tg.ERR_NO_KERNEL
     # depth is bounded only by the budget
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 12, L) == tg.OK

@@ -65,6 +65,8 @@ CONFIGS = [
     ((128, 96, 32), 1),
     ((256, 256, 64), 3),
     ((128, 32, 64), 5),
+    ((128, 128, 128), 3),
+    ((256, 96, 128), 2),
 ]
 SHAPES = [(300, 200, 136), (257, 96, 72), (129, 264, 1032), (1, 32, 8), (64, 512, 16)]
 
@@ -93,6 +95,8 @@ def test_integer_inputs_bit_exact(cuda_lib, block, stages, dtype):
 # ------------------------------------------------------------ CTA-pair mode
 
 PAIR_CONFIGS = [
+    ((256, 256, 128), 3),
+    ((256, 224, 128), 3),
     ((256, 256, 64), 4),
     ((256, 224, 64), 6),
     ((256, 128, 32), 3),

@@ -40,6 +40,7 @@ def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=F
     ((128, 256, 64), (1, 2, 3, 4)),
     ((256, 128, 64), (1, 2, 3)),
     ((128, 64, 16), (1, 2, 4, 8)),
+    ((128, 128, 128), (1, 2, 3)),
 ])
 @pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("bf16", "bf16")])
 def test_bit_identical_across_stages(cuda_lib, block, stage_list, dtype, out):
@@ -54,7 +55,8 @@ def test_bit_identical_across_stages_4096(cuda_lib):
         assert torch.equal(bits(C), bits(res[0]))
 
 
-@pytest.mark.parametrize("block,stage_list", [((256, 256, 64), (1, 2, 4, 6)), ((256, 128, 32), (1, 3, 8))])
+@pytest.mark.parametrize("block,stage_list", [((256, 256, 64), (1, 2, 4, 6)), ((256, 128, 32), (1, 3, 8)),
+                                              ((256, 224, 128), (1, 2, 3))])
 def test_bit_identical_across_stages_pair(cuda_lib, block, stage_list):
     res = outputs_over_stages(cuda_lib, 1000, 1040, 2056, "bf16", "f32", block, stage_list, seed=78, pair=True)
     for s, C in zip(stage_list[1:], res[1:]):
