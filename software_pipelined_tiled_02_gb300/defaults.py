@@ -13,37 +13,45 @@ pages say of cost models; the sweep decides.
 from __future__ import annotations
 
 # (M, N, K, operand dtype, out dtype) -> (block, num_stages[, cta_pair[, split_k]]);
-# dtype codes 0 f16, 1 bf16, 2 f32.
+# dtype codes 0 f16, 1 bf16, 2 f32.  The figures are same-GPU, interleaved
+# timings against the runner-up.
 FROZEN = {
-    (4096, 4096, 4096, 0, 0): ((256, 224, 64), 3),      # 1584 TFLOP/s
-    (8192, 8192, 8192, 1, 1): ((256, 256, 64), 3),      # 1849 TFLOP/s
-    (4000, 3000, 5000, 0, 2): ((256, 192, 64), 3),      # 988 TFLOP/s
-    (512, 512, 32768, 0, 2): ((128, 128, 64), 6, False, 9),  # 484 TFLOP/s; 107 unsplit (16 tiles for 152 SMs)
+    (4096, 4096, 4096, 0, 0): ((256, 224, 64), 3),              # 1622 TFLOP/s; pair 256x224x128: 1622
+    (8192, 8192, 8192, 1, 1): ((256, 256, 128), 3, True),       # 1753 vs 1692 for one CTA 256x256x64
+    (4000, 3000, 5000, 0, 2): ((256, 224, 64), 5, True),        # 1099 vs 988 for one CTA 256x192x64
+    (512, 512, 32768, 0, 2): ((128, 128, 64), 6, False, 9),     # 484 TFLOP/s; 107 unsplit (16 tiles for 152 SMs)
     (128, 128, 128, 0, 2): ((128, 128, 32), 3),
 }
 
-# Candidate tiles with their depth and relative steady-state throughput per
-# SM (measured at full waves on GB300, 256x256 = 1).
+# Candidate tiles: (block, depth, relative steady-state throughput per SM
+# measured at full waves on GB300 with one CTA 256x256 = 1, CTA pair).  A
+# pair computes one 256-row tile on two SMs.
 CANDIDATES = (
-    ((256, 256, 64), 3, 1.00),
-    ((256, 224, 64), 3, 0.98),
-    ((256, 192, 64), 3, 0.90),
-    ((128, 256, 64), 4, 0.90),
-    ((128, 224, 64), 4, 0.86),
-    ((256, 128, 64), 4, 0.80),
-    ((128, 128, 64), 4, 0.60),
-    ((128, 64, 64), 4, 0.35),
+    ((256, 256, 128), 3, 1.04, True),
+    ((256, 224, 64), 5, 1.00, True),
+    ((256, 256, 64), 3, 1.00, False),
+    ((256, 224, 64), 3, 0.98, False),
+    ((256, 192, 64), 3, 0.90, False),
+    ((128, 256, 64), 4, 0.90, False),
+    ((128, 224, 64), 4, 0.86, False),
+    ((256, 128, 64), 4, 0.80, False),
+    ((128, 128, 64), 4, 0.60, False),
+    ((128, 64, 64), 4, 0.35, False),
 )
 
 DEFAULT_SMS = 152
 
 
-def estimate(M: int, N: int, K: int, block, rel: float, num_sms: int = DEFAULT_SMS) -> float:
-    """Relative makespan of a persistent launch of this tile (arbitrary units)."""
+def estimate(M: int, N: int, K: int, block, rel: float, num_sms: int = DEFAULT_SMS, pair: bool = False) -> float:
+    """Relative makespan of a persistent launch of this tile (arbitrary units).
+
+    A pair works on one tile with two SMs: half as many tiles run at once,
+    each in half the time."""
     bm, bn, _ = block
     tiles = -(-M // bm) * -(-N // bn)
-    waves = -(-tiles // num_sms)
-    return waves * bm * bn * max(K, 1) / rel
+    slots = num_sms // 2 if pair else num_sms
+    waves = -(-tiles // slots)
+    return waves * bm * bn * max(K, 1) / (2 if pair else 1) / rel
 
 
 def choose(M: int, N: int, K: int, dtype: int, out_dtype: int, num_sms: int = DEFAULT_SMS) -> dict:
@@ -52,5 +60,5 @@ def choose(M: int, N: int, K: int, dtype: int, out_dtype: int, num_sms: int = DE
     if hit is not None:
         return {"block": hit[0], "num_stages": hit[1], "cta_pair": hit[2] if len(hit) > 2 else False,
                 "split_k": hit[3] if len(hit) > 3 else 1}
-    best = min(CANDIDATES, key=lambda c: (estimate(M, N, K, c[0], c[2], num_sms), -c[2]))
-    return {"block": best[0], "num_stages": best[1], "cta_pair": False, "split_k": 1}
+    best = min(CANDIDATES, key=lambda c: (estimate(M, N, K, c[0], c[2], num_sms, c[3]), -c[2]))
+    return {"block": best[0], "num_stages": best[1], "cta_pair": best[3], "split_k": 1}
