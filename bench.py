@@ -114,9 +114,15 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
-def recorded_traffic(workload):
+def config_key(block, stages, pair, split_k):
+    """The launch configuration as the ncu summaries record it."""
+    return f"{block[0]},{block[1]},{block[2]} S{stages} pair{int(bool(pair))} split{int(split_k)}"
+
+
+def recorded_traffic(workload, config=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    on the current kernel source and, when given, the same launch
+    configuration (see config_key); else None."""
     path = os.path.join(PROFILES, f"tgemm_kernel_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -127,6 +133,8 @@ def recorded_traffic(workload):
                 k, v = line[2:].split(":", 1)
                 fields[k.strip()] = v.strip().strip("`")
     if fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    if config is not None and fields.get("config") != config:
         return None
     try:
         return int(float(fields["dram_bytes_per_launch"]))
@@ -400,7 +408,7 @@ def run_ours(args, w, world, rank, local):
         peak, peak_src = FALLBACK_PEAK_TFLOPS, "fallback"
     achieved = flops / (mean_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": recorded_traffic(args.workload),
+                "traffic": recorded_traffic(args.workload, config_key(block, stages, pair, info["split_k"])),
                 "peak_source": f"{peak_src} dense bf16 burst (fp16 runs at the bf16 rate: nominal ratio 1)",
                 "kernel": ("tgemm_kernel + splitk_reduce_kernel, timed together per step" if info["split_k"] > 1
                            else "tgemm_kernel"), "flops_per_launch": flops,

@@ -86,3 +86,14 @@ def test_recorded_traffic_requires_current_kernel(tmp_path, monkeypatch):
     p.write_text("- kernel_source_sha256: `deadbeef`\n- dram_bytes_per_launch: 1234\n")
     assert bench.recorded_traffic("wl") is None
     assert bench.recorded_traffic("absent") is None
+
+
+def test_recorded_traffic_requires_same_launch_config(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    key = bench.config_key((256, 224, 64), 3, False, 1)
+    assert key == "256,224,64 S3 pair0 split1"
+    p = tmp_path / "tgemm_kernel_wl.md"
+    p.write_text(f"- kernel_source_sha256: `{bench.kernel_source_hash()}`\n- config: `{key}`\n"
+                 "- dram_bytes_per_launch: 99\n")
+    assert bench.recorded_traffic("wl", key) == 99
+    assert bench.recorded_traffic("wl", bench.config_key((256, 224, 128), 3, True, 1)) is None
