@@ -155,7 +155,8 @@ def test_pair_full_size_sampled(cuda_lib, name, block, stages):
 # ------------------------------------------------------------ split-K
 
 SPLIT_CONFIGS = [((128, 128, 64), 4, 4, False), ((128, 64, 32), 3, 7, False), ((256, 128, 64), 3, 3, False),
-                 ((256, 256, 64), 4, 2, True), ((128, 32, 16), 2, 64, False)]
+                 ((256, 256, 64), 4, 2, True), ((128, 32, 16), 2, 64, False), ((128, 128, 128), 3, 3, False),
+                 ((256, 224, 128), 2, 2, True)]
 
 
 @pytest.mark.parametrize("block,stages,splits,pair", SPLIT_CONFIGS, ids=lambda v: str(v))

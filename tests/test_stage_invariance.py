@@ -83,3 +83,21 @@ def test_bit_identical_across_prefetch_distances(cuda_lib):
         assert torch.equal(bits(C), bits(res[0]))
     rc, h = cuda_lib.tgemm_plan_ex(M, N, K, "f16", "f32", 128, 128, 32, 4, prefetch=5)
     assert rc == cuda_lib.ERR_INVALID_ARG and h is None
+
+
+def test_bit_identical_across_prefetch_distances_two_panel_pair(cuda_lib):
+    # The same with 128-column k-blocks (two K-panels per slot) in CTA pairs.
+    M, N, K = 1000, 1040, 2056
+    A, B = inputs.operands(80, M, N, K, "bf16", "normal")
+    dA = inputs.bits_to_torch(A, "bf16").cuda()
+    dB = inputs.bits_to_torch(B, "bf16").cuda()
+    res = []
+    for D in (1, 2, 3):
+        plan = cuda_lib.Plan(M, N, K, "bf16", "bf16", (256, 224, 128), 3, pair=True, prefetch=D)
+        C = plan.run(dA, dB)
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+        res.append(C)
+        plan.close()
+    for C in res[1:]:
+        assert torch.equal(bits(C), bits(res[0]))

@@ -27,6 +27,7 @@ TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
     ((300, 200, 136), "f16", "f32", (128, 128, 32), 3),
     ((1000, 1040, 2056), "bf16", "bf16", (256, 224, 64), 3),
     ((4096, 4096, 4096), "f16", "f16", (256, 224, 64), 3),
+    ((520, 704, 5000), "f16", "f32", (128, 128, 128), 3),
 ])
 def test_noalloc_matches_plan_entry_point_twice(cuda_lib, shape, dtype, out, block, stages):
     tg = cuda_lib
