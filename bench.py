@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s (2MNK/t) at fp16 4096³ and % of GB300 dense tensor peak"
 FALLBACK_PEAK_TFLOPS = 1900.0
+FALLBACK_PEAK_GBS = 6800.0
 L2_FLUSH_BYTES = 256 * 1024 * 1024
 CSRC = os.path.join(ROOT, "software_pipelined_tiled_02_gb300", "csrc")
 PROFILES = os.path.join(ROOT, "profiles")
@@ -94,6 +95,33 @@ def aggregate(per_rank_flops, max_seconds, world):
     if max_seconds <= 0:
         return 0.0
     return per_rank_flops * world / max_seconds / 1e12
+
+
+def roofline_for(flops, algo_bytes, seconds, peaks):
+    """The roofline object of one launch.  The bound is the one the launch's
+    arithmetic intensity (FLOP per algorithmic byte) falls under: HBM below
+    the ridge peak_flops / peak_bandwidth, the tensor pipe above it.  Both
+    fractions are reported; `achieved`, `peak`, `unit` and `frac` follow the
+    bound."""
+    if peaks and peaks.get("bf16_tflops"):
+        tflops, t_src = float(peaks["bf16_tflops"]), "measured"
+    else:
+        tflops, t_src = FALLBACK_PEAK_TFLOPS, "fallback"
+    if peaks and peaks.get("hbm_gbs"):
+        gbs, g_src = float(peaks["hbm_gbs"]), "measured"
+    else:
+        gbs, g_src = FALLBACK_PEAK_GBS, "fallback"
+    achieved_tf = flops / seconds / 1e12
+    achieved_gbs = algo_bytes / seconds / 1e9
+    ridge = tflops * 1e12 / (gbs * 1e9)
+    intensity = flops / algo_bytes
+    common = {"tensor_frac": achieved_tf / tflops, "hbm_frac": achieved_gbs / gbs,
+              "intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge}
+    if intensity < ridge:
+        return {"bound": "hbm", "achieved": achieved_gbs, "peak": gbs, "unit": "GB/s", "frac": achieved_gbs / gbs,
+                "peak_source": f"{g_src} HBM copy bandwidth", **common}
+    return {"bound": "tensor", "achieved": achieved_tf, "peak": tflops, "unit": "TFLOP/s", "frac": achieved_tf / tflops,
+            "peak_source": f"{t_src} dense bf16 burst (fp16 runs at the bf16 rate: nominal ratio 1)", **common}
 
 
 def measured_peaks():
@@ -401,18 +429,12 @@ def run_ours(args, w, world, rank, local):
 
     clocks = sampler.stop() if sampler else None
 
-    peaks = measured_peaks()
-    if peaks and peaks.get("bf16_tflops"):
-        peak, peak_src = float(peaks["bf16_tflops"]), "measured"
-    else:
-        peak, peak_src = FALLBACK_PEAK_TFLOPS, "fallback"
-    achieved = flops / (mean_ms / 1e3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": recorded_traffic(args.workload, config_key(block, stages, pair, info["split_k"])),
-                "peak_source": f"{peak_src} dense bf16 burst (fp16 runs at the bf16 rate: nominal ratio 1)",
-                "kernel": ("tgemm_kernel + splitk_reduce_kernel, timed together per step" if info["split_k"] > 1
-                           else "tgemm_kernel"), "flops_per_launch": flops,
-                "algorithmic_bytes_per_launch": (M * K + N * K) * 2 + M * N * (4 if w["out"] == "f32" else 2)}
+    algo_bytes = (M * K + N * K) * 2 + M * N * (4 if w["out"] == "f32" else 2)
+    roofline = roofline_for(flops, algo_bytes, mean_ms / 1e3, measured_peaks())
+    roofline.update({"traffic": recorded_traffic(args.workload, config_key(block, stages, pair, info["split_k"])),
+                     "kernel": ("tgemm_kernel + splitk_reduce_kernel, timed together per step"
+                                if info["split_k"] > 1 else "tgemm_kernel"),
+                     "flops_per_launch": flops, "algorithmic_bytes_per_launch": algo_bytes})
 
     line = None
     if rank == 0:

@@ -97,3 +97,20 @@ def test_recorded_traffic_requires_same_launch_config(tmp_path, monkeypatch):
                  "- dram_bytes_per_launch: 99\n")
     assert bench.recorded_traffic("wl", key) == 99
     assert bench.recorded_traffic("wl", bench.config_key((256, 224, 128), 3, True, 1)) is None
+
+
+def test_roofline_bound_follows_arithmetic_intensity():
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0}  # ridge 250 FLOP/B
+    # 4096^3 fp16 -> fp16: 1365 FLOP/B, tensor-bound
+    f, b = 2 * 4096 ** 3, 3 * 4096 * 4096 * 2
+    r = bench.roofline_for(f, b, 1e-4, peaks)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["achieved"] == pytest.approx(f / 1e-4 / 1e12) and r["frac"] == pytest.approx(r["achieved"] / 2000.0)
+    # 512x512x32768 fp16 -> fp32: 252 FLOP/B ... just above this ridge; 200 FLOP/B is below it
+    r = bench.roofline_for(200.0 * 1e9, 1e9, 1e-3, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(1e9 / 1e-3 / 1e9) and r["frac"] == pytest.approx(1000.0 / 8000.0)
+    assert r["tensor_frac"] == pytest.approx(200.0 / 2000.0)
+    # without measured peaks the recipe's fallbacks are used
+    r = bench.roofline_for(f, b, 1e-4, None)
+    assert r["peak"] == bench.FALLBACK_PEAK_TFLOPS and r["peak_source"].startswith("fallback")
