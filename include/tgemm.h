@@ -24,8 +24,10 @@
  * value documented below; nothing throws across this boundary and nothing
  * aborts the process.  Arguments are checked before anything is launched.
  *
- * Threads.  A plan may be used from one host thread at a time.  Different
- * plans are independent.
+ * Threads and streams.  A plan may be used from one host thread at a time.
+ * Different plans are independent.  Launches of one plan on different streams
+ * may overlap, except with split_k > 1: those share the plan's workspace, so
+ * they must be ordered (one stream, or events between them).
  */
 #ifndef TGEMM_H
 #define TGEMM_H
@@ -116,7 +118,8 @@ int tgemm_validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, in
  * by the caller (free it with tgemm_destroy); on failure *out is NULL.  The
  * pages' analogue is matmul(M, N, K, block_M, block_N, block_K, num_stages,
  * ...) of chapter 11 section 3.5; its `threads` argument has no counterpart
- * because the kernel's warp roles fix the block at 192 threads.
+ * because the kernel's warp roles fix the block at 320 threads (a TMA producer
+ * warp, an MMA warp and eight epilogue warps).
  */
 int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
                int block_M, int block_N, int block_K, int num_stages);
@@ -265,7 +268,10 @@ int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
                       int block_K, int num_stages, const void *A, const void *B, void *C, tgemm_stream_t stream,
                       int *status);
 
-/* Free a plan and its status word.  NULL is accepted (no-op). */
+/* Free a plan, its status word and its split-K workspace.  The device memory
+ * goes back through cudaFree, which first waits for the device to finish its
+ * work, so launches of the plan still in flight complete before it is freed.
+ * NULL is accepted (no-op). */
 int tgemm_destroy(tgemm_plan_t plan);
 
 /* Static text for a status code (never NULL). */

@@ -13,6 +13,7 @@ plus a ``Plan`` wrapper and ``gemm()``.
 
 from __future__ import annotations
 
+import collections
 import ctypes
 import os
 import threading
@@ -314,7 +315,11 @@ class Plan:
             pass
 
 
-_plans: dict = {}
+# gemm()'s plans, least recently used first.  Bounded, because every plan holds
+# device memory (its status word, and a workspace when K is split).
+_plans: "collections.OrderedDict" = collections.OrderedDict()
+_plans_lock = threading.Lock()
+_PLANS_MAX = 64
 
 
 def default_config(M, N, K, dtype="f16", out_dtype=None) -> dict:
@@ -345,7 +350,14 @@ def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=Non
     pair = bool(pair)
     split_k = int(split_k or 1)
     key = (M, N, K, dt, odt, tuple(block), num_stages, pair, split_k, A.device.index)
-    plan = _plans.get(key)
-    if plan is None:
-        plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages, pair=pair, split_k=split_k)
-    return plan.run(A, B, out, stream)
+    # A plan serves one host thread at a time (it caches tensor maps per pointer
+    # triple), so the lookup and the enqueue happen under the lock.
+    with _plans_lock:
+        plan = _plans.get(key)
+        if plan is None:
+            plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages, pair=pair, split_k=split_k)
+            while len(_plans) > _PLANS_MAX:
+                _plans.popitem(last=False)[1].close()
+        else:
+            _plans.move_to_end(key)
+        return plan.run(A, B, out, stream)

@@ -23,10 +23,11 @@
 //  * num_stages = 1 is the unpipelined control of section 1.1 (copy and math
 //    serialise on the single slot).
 //
-// Warp roles (192 threads, one CTA per SM, persistent over output tiles):
-//   warp 0      TMA producer (one thread)
-//   warp 1      TMEM allocator and tcgen05.mma issuer (one thread)
-//   warps 2..5  epilogue: TMEM -> registers -> swizzled shared staging -> TMA store
+// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer (one thread issues)
+//   warp 1      TMEM allocator and tcgen05.mma issuer (one thread issues)
+//   warps 2..9  epilogue, two warps per TMEM lane quarter: TMEM -> registers ->
+//               swizzled shared staging -> TMA store
 // The accumulator is double-buffered in TMEM when it fits, so the epilogue of
 // tile i overlaps the main loop of tile i+1.  The summation order inside a
 // tile depends only on the tile shape (k-block by k-block, 16 at a time), never
