@@ -1,0 +1,66 @@
+"""A seeded random sweep of shapes and launch configurations against the oracle.
+
+Each case draws operand and output dtypes, a ragged shape (the only
+constraint is the 16-byte row-pitch rule), a tile, a depth the shared memory
+admits, CTA pairs, a K split and a producer lead.  It then compares the
+kernel's C with the fp64 oracle element by element, to the tolerance of
+oracle.check.  The draws come from one fixed seed, so a failure names a
+reproducible case.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from software_pipelined_tiled_02_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+SINGLE_TILES = [(128, 128, 32), (128, 256, 64), (256, 128, 64), (128, 64, 16), (256, 224, 64), (128, 128, 128),
+                (256, 96, 128), (128, 32, 64), (256, 256, 64), (128, 192, 64)]
+PAIR_TILES = [(256, 256, 128), (256, 224, 128), (256, 256, 64), (256, 128, 32), (256, 64, 16), (256, 32, 64),
+              (256, 192, 128), (256, 160, 64)]
+N_CASES = 160
+
+
+def draw_cases(tg, n=N_CASES, seed=20261202):
+    rng = np.random.default_rng(seed)
+    limit = tg.tgemm_smem_limit()
+    cases = []
+    while len(cases) < n:
+        dtype = str(rng.choice(["f16", "bf16"]))
+        out = str(rng.choice(["f32", dtype]))
+        pair = bool(rng.random() < 0.35)
+        block = PAIR_TILES[rng.integers(len(PAIR_TILES))] if pair else SINGLE_TILES[rng.integers(len(SINGLE_TILES))]
+        M = int(rng.integers(1, 521))
+        n_align = 4 if out == "f32" else 8
+        N = int(rng.integers(1, 521 // n_align + 1)) * n_align
+        K = int(rng.integers(1, 1041 // 8 + 1)) * 8
+        split = int(rng.choice([1, 1, 1, 2, 3, 5]))
+        stages = int(rng.integers(1, 9))
+        if tg.tgemm_validate_ex(M, N, K, dtype, out, *block, stages, limit, cta_pair=int(pair),
+                                split_k=split) != tg.OK:
+            continue
+        prefetch = int(rng.integers(1, stages + 1)) if rng.random() < 0.25 else 0
+        cases.append((M, N, K, dtype, out, block, stages, pair, split, prefetch, int(rng.integers(1 << 30))))
+    return cases
+
+
+def test_random_sweep_matches_oracle(cuda_lib):
+    tg = cuda_lib
+    failures = []
+    for i, (M, N, K, dtype, out, block, stages, pair, split, prefetch, seed) in enumerate(draw_cases(tg)):
+        A, B = inputs.operands(seed, M, N, K, dtype, "normal")
+        plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair, split_k=split, prefetch=prefetch)
+        C = torch.full((M, N), float("nan"), dtype=TORCH[out], device="cuda")
+        plan.run(inputs.bits_to_torch(A, dtype).cuda(), inputs.bits_to_torch(B, dtype).cuda(), C)
+        torch.cuda.synchronize()
+        code = plan.status()[0]
+        plan.close()
+        R, S = oracle.gemm(A, B, dtype)
+        ok, worst, idx = oracle.check(C.float().cpu().double().numpy(), R, S, out)
+        if code != 0 or not ok:
+            failures.append((i, (M, N, K, dtype, out, block, stages, pair, split, prefetch, seed), code, worst))
+    assert not failures, failures
