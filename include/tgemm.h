@@ -61,7 +61,9 @@ enum tgemm_status_code {
     TGEMM_ERR_NO_KERNEL = 5,         /* tile shape the kernel does not implement */
     TGEMM_ERR_ARCH = 6,              /* current device is not compute capability 10.3 */
     TGEMM_ERR_CUDA = 7,              /* a CUDA runtime or driver call failed */
-    TGEMM_ERR_TIMEOUT = 8            /* a pipeline wait inside the kernel ran out of time */
+    TGEMM_ERR_TIMEOUT = 8,           /* a pipeline wait inside the kernel ran out of time */
+    TGEMM_ERR_CHECK = 9              /* an internal bounds or alignment check failed; only a
+                                        build with TGEMM_DEBUG_CHECKS=1 makes these checks */
 };
 
 /*

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(HERE, "libtgemm.so")
 
 F16, BF16, F32 = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DTYPE, ERR_ALIGNMENT, ERR_SMEM_BUDGET, ERR_NO_KERNEL, ERR_ARCH, ERR_CUDA, \
-    ERR_TIMEOUT = range(9)
+    ERR_TIMEOUT, ERR_CHECK = range(10)
 _DT_NAMES = {"f16": F16, "bf16": BF16, "f32": F32}
 
 SYMBOLS = ("tgemm_smem_bound", "tgemm_smem_bytes", "tgemm_smem_limit", "tgemm_validate", "tgemm_plan",
@@ -62,12 +62,15 @@ _lock = threading.Lock()
 _lib = None
 
 
-def load(path: str = LIB_PATH):
-    """Load ``libtgemm.so`` (raises if it is absent: there is no fallback)."""
+def load(path: str | None = None):
+    """Load ``libtgemm.so`` (raises if it is absent: there is no fallback).
+    The environment variable ``TGEMM_LIB`` names another build of the same
+    library, such as the debug-check build ``libtgemm_debug.so``."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
+        path = path or os.environ.get("TGEMM_LIB") or LIB_PATH
         if not os.path.exists(path):
             raise RuntimeError(f"libtgemm.so not built at {path}; run software_pipelined_tiled_02_gb300/build.py "
                                "or __graft_entry__.build()")

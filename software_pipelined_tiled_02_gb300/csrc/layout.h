@@ -18,6 +18,7 @@ enum : int {
     kErrArch = 6,
     kErrCuda = 7,
     kErrTimeout = 8,
+    kErrCheck = 9,  // an internal bounds or alignment check failed (debug-check builds only)
 };
 
 enum : int { kF16 = 0, kBF16 = 1, kF32 = 2 };

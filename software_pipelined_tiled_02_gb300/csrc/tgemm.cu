@@ -97,6 +97,26 @@ __device__ __forceinline__ void report(const Params &p, int code, int role, int 
     }
 }
 
+// Debug-check builds (TGEMM_DEBUG_CHECKS=1) test every shared-memory, tensor-
+// memory and TMA address the kernel forms against the plan's layout before the
+// access.  A failed check records TGEMM_ERR_CHECK with the role and the
+// iteration, raises the CTA's abort flag and skips the access, so a bug shows
+// up as a status code, never as a fault.  Release builds compile the checks
+// away.
+#ifndef TGEMM_DEBUG_CHECKS
+#define TGEMM_DEBUG_CHECKS 0
+#endif
+
+__device__ __forceinline__ bool check(bool ok, const Params &p, volatile int *abort, int role, int iter)
+{
+    if (TGEMM_DEBUG_CHECKS && !ok) {
+        report(p, kErrCheck, role, iter);
+        *abort = 1;
+        return false;
+    }
+    return true;
+}
+
 // Bounded wait for the phase of parity `parity` of `bar`.  Returns false when
 // the CTA has aborted (if honour_abort) or when the watchdog expires; the
 // latter is recorded and raises the CTA's abort flag.
@@ -229,7 +249,15 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
                 break;
             }
             tc_fence_after();
-            if (lane == 0) {
+            // slot s's operands lie inside the A and B rings; the accumulator inside TMEM
+            const bool in_range =
+                check(uint32_t(ad & 0x3FFFu) << 4 >= c.sA && ((uint32_t(ad & 0x3FFFu) << 4) + p.a_slot) <=
+                                                                  c.sA + uint32_t(S) * p.a_slot &&
+                          uint32_t(bd & 0x3FFFu) << 4 >= c.sB &&
+                          ((uint32_t(bd & 0x3FFFu) << 4) + p.b_slot) <= c.sB + uint32_t(S) * p.b_slot &&
+                          a * p.acc_cols + MH * p.bn <= p.tmem_cols && kb1 <= p.num_kb,
+                      p, abort, 1, it);
+            if (lane == 0 && in_range) {
                 const uint32_t first = kb != kb0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < NK; ++kk) {
@@ -388,7 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                         if (issued >= D) phd ^= 1u;
                     }
                 }
-                if (lane == 0) {
+                const bool in_range =
+                    check(s < S && (kb * p.bk * 2) % 16 == 0 && kb < p.num_kb && w.mb < p.tiles_m &&
+                              w.nb < p.tiles_n && int(p.panels) * int(p.a_panel16 << 4) <= int(p.a_slot) &&
+                              int(p.panels) * int(p.b_panel16 << 4) <= int(p.b_slot),
+                          p, abort, 0, issued);
+                if (lane == 0 && in_range) {
                     const uint32_t a_dst = sA + uint32_t(s) * p.a_slot, b_dst = sB + uint32_t(s) * p.b_slot;
                     if constexpr (PAIR) {
                         const uint32_t fb = full_leader + 8u * uint32_t(s);
@@ -467,6 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                     const int col0 = n0 + c * kEpiCols;
                     if (col0 >= p.N) break;  // warp-uniform
                     if ((idx++ & 1) != sub) continue;  // the other warp of this quarter takes it
+                    // the chunk's TMEM columns, staging buffer and store box lie inside their regions
+                    if (!check(a * p.acc_cols + h * p.bn + (c + 1) * kEpiCols <= p.tmem_cols &&
+                                   uint32_t((warp - 1) * nbuf) * p.c_buf_bytes <= p.off_bar - p.off_c &&
+                                   col0 % 8 == 0 && w.row_off + row0 >= 0,
+                               p, abort, 2, tiles_done))
+                        continue;
                     uint32_t v[32];
                     if (p.num_kb > 0) {
                         tmem_ld_32x32b_x32(tmem + lane_base + uint32_t(a * p.acc_cols + h * p.bn + c * kEpiCols), v);
@@ -1123,6 +1162,7 @@ const char *tgemm_strerror(int code)
     case kErrArch: return "device is not compute capability 10.3 (GB300)";
     case kErrCuda: return "CUDA runtime or driver call failed";
     case kErrTimeout: return "a pipeline wait in the kernel exceeded the watchdog limit";
+    case kErrCheck: return "an internal bounds or alignment check failed (debug-check build)";
     default: return "unknown status code";
     }
 }
