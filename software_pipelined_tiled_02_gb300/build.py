@@ -67,5 +67,26 @@ def build(force: bool = False, verbose: bool = False, debug: bool = False) -> st
     return lib
 
 
+def build_all(force: bool = False) -> list[str]:
+    """Compile the release and the debug-check library side by side (two nvcc
+    processes), skipping whichever is up to date."""
+    jobs = []
+    for debug, lib in ((False, LIB), (True, LIB_DEBUG)):
+        if force or not up_to_date(lib):
+            tmp = lib + f".{os.getpid()}.tmp"
+            jobs.append((lib, tmp, subprocess.Popen(command(tmp, debug=debug), stdout=subprocess.PIPE,
+                                                    stderr=subprocess.STDOUT, text=True)))
+    errors = []
+    for lib, tmp, proc in jobs:
+        out, _ = proc.communicate()
+        if proc.returncode != 0:
+            errors.append(f"nvcc failed for {os.path.basename(lib)}:\n{out}")
+        else:
+            os.replace(tmp, lib)
+    if errors:
+        raise RuntimeError("\n".join(errors))
+    return [LIB, LIB_DEBUG]
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))
