@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--pair", type=int, choices=(0, 1), default=None,
                     help="1: CTA pairs (clusters of 2) share each 256-row tile (default: tuned table)")
     ap.add_argument("--split-k", type=int, default=None, help="K splits per tile (default: tuned table)")
+    ap.add_argument("--group-m", type=int, default=None,
+                    help="M-blocks per raster group of the persistent schedule (default: tuned table; 0 = 8)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -142,9 +144,10 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
-def config_key(block, stages, pair, split_k):
+def config_key(block, stages, pair, split_k, group_m=8):
     """The launch configuration as the ncu summaries record it."""
-    return f"{block[0]},{block[1]},{block[2]} S{stages} pair{int(bool(pair))} split{int(split_k)}"
+    return (f"{block[0]},{block[1]},{block[2]} S{stages} pair{int(bool(pair))} split{int(split_k)} "
+            f"group{int(group_m) or 8}")
 
 
 def recorded_traffic(workload, config=None):
@@ -324,9 +327,11 @@ def run_ours(args, w, world, rank, local):
         stages = args.stages or 4
         pair = bool(args.pair)
         split_k = args.split_k or 1
+        group_m = args.group_m or 0
     else:
         cfg = tg.default_config(M, N, K, w["dtype"], w["out"])
         block, stages, pair, split_k = cfg["block"], cfg["num_stages"], cfg["cta_pair"], cfg["split_k"]
+        group_m = cfg["group_m"] if args.group_m is None else args.group_m
         if args.stages:
             stages = args.stages
         if args.pair is not None:
@@ -339,7 +344,7 @@ def run_ours(args, w, world, rank, local):
     dA, dB = hA.to(dev), hB.to(dev)
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[w["out"]]
     dC = torch.empty((M, N), dtype=tdt, device=dev)
-    plan = tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k)
+    plan = tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k, group_m=group_m)
     info = plan.info
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -389,7 +394,8 @@ def run_ours(args, w, world, rank, local):
         # as a caller streaming independent GEMMs would run them.
         pA, pB = hA.pin_memory(), hB.pin_memory()
         pCs = [torch.empty((M, N), dtype=tdt).pin_memory() for _ in range(2)]
-        plans = [plan, tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k)]
+        plans = [plan, tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k,
+                               group_m=group_m)]
         bufs = [(dA, dB, dC), (torch.empty_like(dA), torch.empty_like(dB), torch.empty_like(dC))]
         streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
         torch.cuda.synchronize(dev)
@@ -431,7 +437,8 @@ def run_ours(args, w, world, rank, local):
 
     algo_bytes = (M * K + N * K) * 2 + M * N * (4 if w["out"] == "f32" else 2)
     roofline = roofline_for(flops, algo_bytes, mean_ms / 1e3, measured_peaks())
-    roofline.update({"traffic": recorded_traffic(args.workload, config_key(block, stages, pair, info["split_k"])),
+    roofline.update({"traffic": recorded_traffic(args.workload,
+                                                 config_key(block, stages, pair, info["split_k"], group_m)),
                      "kernel": ("tgemm_kernel + splitk_reduce_kernel, timed together per step"
                                 if info["split_k"] > 1 else "tgemm_kernel"),
                      "flops_per_launch": flops, "algorithmic_bytes_per_launch": algo_bytes})
@@ -445,7 +452,7 @@ def run_ours(args, w, world, rank, local):
                 "warmup": args.warmup, "ms_per_step": max_mean_ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
                 "config": dict(config_block(args, w, block, stages), cta_pair=int(pair),
-                               split_k=int(info["split_k"])), "roofline": roofline,
+                               split_k=int(info["split_k"]), group_m=int(group_m) or 8), "roofline": roofline,
                 "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": args.steps * (2 if info["split_k"] > 1 else 1), "clocks": clocks,
                 "plan": {k: info[k] for k in ("grid", "num_tiles", "smem_bytes", "tmem_columns", "acc_stages")},

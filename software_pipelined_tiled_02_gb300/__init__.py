@@ -233,13 +233,13 @@ class Plan:
     """A validated GEMM configuration on the current CUDA device."""
 
     def __init__(self, M, N, K, dtype="f16", out_dtype=None, block=(128, 256, 64), num_stages=4, pair=False,
-                 split_k=1, prefetch=0):
+                 split_k=1, prefetch=0, group_m=0):
         dtype = _dt(dtype)
         out_dtype = dtype if out_dtype is None else _dt(out_dtype)
         bm, bn, bk = block
-        if pair or split_k > 1 or prefetch:
+        if pair or split_k > 1 or prefetch or group_m:
             rc, h = tgemm_plan_ex(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages, cta_pair=int(bool(pair)),
-                                  split_k=int(split_k), prefetch=int(prefetch))
+                                  split_k=int(split_k), prefetch=int(prefetch), group_m=int(group_m))
         else:
             rc, h = tgemm_plan(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages)
         if rc != OK:
@@ -326,13 +326,14 @@ _PLANS_MAX = 64
 
 
 def default_config(M, N, K, dtype="f16", out_dtype=None) -> dict:
-    """The tuned default {block, num_stages, cta_pair, split_k} for a shape."""
+    """The tuned default {block, num_stages, cta_pair, split_k, group_m} for a shape."""
     from . import defaults
 
     return defaults.choose(M, N, K, _dt(dtype), _dt(dtype) if out_dtype is None else _dt(out_dtype))
 
 
-def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=None, pair=None, split_k=None):
+def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=None, pair=None, split_k=None,
+         group_m=None):
     """``A[M,K] . B[N,K]^T`` on the GPU through ``libtgemm.so``.
 
     ``out_dtype`` defaults to the operand dtype; ``torch.float32`` returns the
@@ -350,15 +351,18 @@ def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=Non
         num_stages = num_stages or cfg["num_stages"]
         pair = cfg["cta_pair"] if pair is None else pair
         split_k = cfg["split_k"] if split_k is None else split_k
+        group_m = cfg["group_m"] if group_m is None else group_m
     pair = bool(pair)
     split_k = int(split_k or 1)
-    key = (M, N, K, dt, odt, tuple(block), num_stages, pair, split_k, A.device.index)
+    group_m = int(group_m or 0)
+    key = (M, N, K, dt, odt, tuple(block), num_stages, pair, split_k, group_m, A.device.index)
     # A plan serves one host thread at a time (it caches tensor maps per pointer
     # triple), so the lookup and the enqueue happen under the lock.
     with _plans_lock:
         plan = _plans.get(key)
         if plan is None:
-            plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages, pair=pair, split_k=split_k)
+            plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages, pair=pair, split_k=split_k,
+                                      group_m=group_m)
             while len(_plans) > _PLANS_MAX:
                 _plans.popitem(last=False)[1].close()
         else:

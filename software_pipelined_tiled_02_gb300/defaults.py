@@ -12,11 +12,12 @@ pages say of cost models; the sweep decides.
 
 from __future__ import annotations
 
-# (M, N, K, operand dtype, out dtype) -> (block, num_stages[, cta_pair[, split_k]]);
-# dtype codes 0 f16, 1 bf16, 2 f32.  The figures are same-GPU, interleaved
+# (M, N, K, operand dtype, out dtype) -> (block, num_stages[, cta_pair[, split_k[, group_m]]]);
+# dtype codes 0 f16, 1 bf16, 2 f32; group_m is the persistent raster's group of
+# M-blocks (0: the library's 8).  The figures are same-GPU, interleaved
 # timings against the runner-up.
 FROZEN = {
-    (4096, 4096, 4096, 0, 0): ((256, 224, 64), 3),              # 1622 TFLOP/s; pair 256x224x128: 1622
+    (4096, 4096, 4096, 0, 0): ((256, 224, 128), 3, True, 1, 2),  # 1643 vs 1607 for one CTA 256x224x64, group 8
     (8192, 8192, 8192, 1, 1): ((256, 256, 128), 3, True),       # 1753 vs 1692 for one CTA 256x256x64
     (4000, 3000, 5000, 0, 2): ((256, 224, 64), 5, True),        # 1099 vs 988 for one CTA 256x192x64
     (512, 512, 32768, 0, 2): ((256, 256, 128), 3, True, 19),    # 514 vs 485 for 128x128x64 S6 split 9; 107 unsplit
@@ -55,10 +56,10 @@ def estimate(M: int, N: int, K: int, block, rel: float, num_sms: int = DEFAULT_S
 
 
 def choose(M: int, N: int, K: int, dtype: int, out_dtype: int, num_sms: int = DEFAULT_SMS) -> dict:
-    """{block, num_stages, cta_pair, split_k} for a problem."""
+    """{block, num_stages, cta_pair, split_k, group_m} for a problem."""
     hit = FROZEN.get((M, N, K, dtype, out_dtype))
     if hit is not None:
         return {"block": hit[0], "num_stages": hit[1], "cta_pair": hit[2] if len(hit) > 2 else False,
-                "split_k": hit[3] if len(hit) > 3 else 1}
+                "split_k": hit[3] if len(hit) > 3 else 1, "group_m": hit[4] if len(hit) > 4 else 0}
     best = min(CANDIDATES, key=lambda c: (estimate(M, N, K, c[0], c[2], num_sms, c[3]), -c[2]))
-    return {"block": best[0], "num_stages": best[1], "cta_pair": best[3], "split_k": 1}
+    return {"block": best[0], "num_stages": best[1], "cta_pair": best[3], "split_k": 1, "group_m": 0}

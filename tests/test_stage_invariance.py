@@ -101,3 +101,22 @@ def test_bit_identical_across_prefetch_distances_two_panel_pair(cuda_lib):
         plan.close()
     for C in res[1:]:
         assert torch.equal(bits(C), bits(res[0]))
+
+
+def test_bit_identical_across_raster_groups(cuda_lib):
+    # group_m only changes which CTA computes which tile, never a sum.
+    M, N, K = 2000, 2080, 1032
+    A, B = inputs.operands(81, M, N, K, "f16", "normal")
+    dA = inputs.bits_to_torch(A, "f16").cuda()
+    dB = inputs.bits_to_torch(B, "f16").cuda()
+    for pair, block in ((False, (256, 224, 64)), (True, (256, 224, 128))):
+        res = []
+        for gm in (1, 2, 8, 16):
+            plan = cuda_lib.Plan(M, N, K, "f16", "f16", block, 3, pair=pair, group_m=gm)
+            C = plan.run(dA, dB)
+            torch.cuda.synchronize()
+            assert plan.status()[0] == 0
+            res.append(C)
+            plan.close()
+        for C in res[1:]:
+            assert torch.equal(bits(C), bits(res[0]))
