@@ -8,6 +8,8 @@ oracle.check.  The draws come from one fixed seed, so a failure names a
 reproducible case.
 """
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -22,7 +24,7 @@ SINGLE_TILES = [(128, 128, 32), (128, 256, 64), (256, 128, 64), (128, 64, 16), (
                 (256, 96, 128), (128, 32, 64), (256, 256, 64), (128, 192, 64)]
 PAIR_TILES = [(256, 256, 128), (256, 224, 128), (256, 256, 64), (256, 128, 32), (256, 64, 16), (256, 32, 64),
               (256, 192, 128), (256, 160, 64)]
-N_CASES = 160
+N_CASES = int(os.environ.get("TGEMM_SWEEP_CASES", "160"))  # more for a longer soak
 
 
 def draw_cases(tg, n=N_CASES, seed=20261202):
