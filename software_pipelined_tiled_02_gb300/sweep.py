@@ -9,8 +9,9 @@ autotuning", restated for this kernel:
   per-block shared-memory budget (section 4.5), here the limit queried from
   the device, never a constant;
 * section 3.5: run every surviving candidate on the same inputs, warm-up then
-  timed repetitions, and check each against a reference (here: sampled
-  entries of the fp64 oracle, to the kernel tolerance);
+  timed repetitions, and check each against the reference program the
+  pages use, torch.matmul on fp32 copies of the operands, at rtol = atol =
+  1e-2 (the fp64 oracle is test infrastructure, kept out of this tool);
 * section 3.8: read the config, not the latency: the winner (lowest median
   time; ties within 1 % go to the smaller shared footprint, then to fewer
   stages) is written to a per-device cache file, and a switch
@@ -33,7 +34,6 @@ import os
 import statistics
 import sys
 
-import numpy as np
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
@@ -104,9 +104,15 @@ def load_cached(device_name: str, workload: str):
 
 
 class Runner:
-    """Times candidates of one workload on the current GPU and checks them."""
+    """Times candidates of one workload on the current GPU and checks them.
 
-    def __init__(self, workload: str, reps: int = 20, warmup: int = 5, check_entries: int = 512):
+    The check is the autotuner's own: the pages compare every candidate with
+    their reference program, ``torch.matmul`` on fp32 copies of the operands,
+    at rtol = atol = 1e-2 (chapter 11, sections 3.5-3.6).  The fp64 oracle is
+    test infrastructure and stays out of this tool.
+    """
+
+    def __init__(self, workload: str, reps: int = 20, warmup: int = 5):
         import torch
 
         self.torch = torch
@@ -121,13 +127,8 @@ class Runner:
         self.C = torch.empty((self.M, self.N), dtype=tdt, device="cuda")
         self.flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
         self.reps, self.warmup = reps, warmup
-        rng = np.random.default_rng(123)
-        self.rows = rng.integers(0, self.M, check_entries)
-        self.cols = rng.integers(0, self.N, check_entries)
-        import oracle
-
-        self.R, self.S = oracle.gemm_entries(self.A, self.B, w["dtype"], self.rows, self.cols)
-        self.oracle = oracle
+        with _no_tf32(torch):
+            self.ref = self.dA.float() @ self.dB.float().t()
 
     def run(self, c: dict) -> dict:
         torch = self.torch
@@ -155,14 +156,30 @@ class Runner:
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1))
         code, _ = plan.status()
-        got = self.C[torch.from_numpy(self.rows).cuda(), torch.from_numpy(self.cols).cuda()].float().cpu().double()
-        ok, worst, _ = self.oracle.check(got.numpy(), self.R, self.S, w["out"])
+        err = (self.C.float() - self.ref).abs()
+        bound = 1e-2 + 1e-2 * self.ref.abs()
+        worst = float((err / bound).max())  # NaN (an unwritten entry) fails the comparison below
+        ok = worst <= 1.0
         med = statistics.median(times)
         row.update(ok=bool(ok and code == tg.OK), worst_error_ratio=worst, median_ms=med, min_ms=min(times),
                    tflops=2.0 * self.M * self.N * self.K / (med * 1e-3) / 1e12, smem_bytes=info["smem_bytes"],
                    smem_bound=info["smem_bound"], grid=info["grid"], tiles=info["num_tiles"])
         plan.close()
         return row
+
+
+class _no_tf32:
+    """Context manager: fp32 matmuls in full precision (no TF32) while it is open."""
+
+    def __init__(self, torch):
+        self.m = torch.backends.cuda.matmul
+
+    def __enter__(self):
+        self.saved = self.m.allow_tf32
+        self.m.allow_tf32 = False
+
+    def __exit__(self, *exc):
+        self.m.allow_tf32 = self.saved
 
 
 def main(argv=None):
