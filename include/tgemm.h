@@ -96,7 +96,9 @@ int tgemm_smem_limit(void);
  * limit, without touching a GPU: the same checks tgemm_plan makes, in the
  * same order, with `smem_limit` standing in for the queried device limit.
  *   - dtype in {F16, BF16}, out_dtype in {F32, dtype}     -> UNSUPPORTED_DTYPE
- *   - M, N >= 0, K >= 0, each < 2^31; num_stages >= 1      -> INVALID_ARG
+ *   - M, N >= 0, K >= 0, each <= 2^31 - 257 (a coordinate
+ *     rounded up to a whole tile stays a 32-bit TMA
+ *     coordinate); num_stages >= 1                         -> INVALID_ARG
  *   - K % 8 == 0, N * out_bytes % 16 == 0 (row pitch)      -> ALIGNMENT
  *   - block_M in {128, 256}; block_N a multiple of 32 in
  *     [32, 256]; block_K in {16, 32, 64, 128} (16-bit
@@ -144,7 +146,9 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
  *     rounds once to C's type.
  *     The order of every sum depends only on the tile shape and s, never on
  *     num_stages, so results stay bit-identical across depths.  For long K
- *     and few output tiles (more SMs than tiles).  At most 64.
+ *     and few output tiles (more SMs than tiles).  At most 64, and the
+ *     workspace rows, s x ceil(M / block_M) x block_M, below 2^31
+ *     (32-bit TMA coordinates); else INVALID_ARG.
  *   prefetch: 0 = num_stages.  1 <= D <= num_stages = the producer issues the
  *     loads of k-block i only after the MMAs of k-block i - D have finished,
  *     i.e. it runs at most D k-blocks ahead whatever the number of buffers.
@@ -161,7 +165,10 @@ typedef struct tgemm_plan_opts {
     int prefetch;
 } tgemm_plan_opts;
 
-/* tgemm_validate with options (NULL = defaults). */
+/* tgemm_validate with options (NULL = defaults): the option ranges above
+ * (cta_pair 0 or 1, group_m 0..4096, split_k 0..64, prefetch 0..num_stages)
+ * give INVALID_ARG, then the checks of tgemm_validate and the split-K
+ * workspace rule, as tgemm_plan_ex makes them. */
 int tgemm_validate_ex(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M,
                       int block_N, int block_K, int num_stages, int64_t smem_limit,
                       const tgemm_plan_opts *opts);

@@ -113,6 +113,7 @@ inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out
 // Every check of tgemm_validate, in the documented order.
 // Largest number of K splits a plan accepts.
 constexpr int kMaxSplits = 64;
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1 - 256;  // largest M, N or K
 
 // Effective number of K splits: at least one k-block per split.
 inline int effective_splits(int64_t K, int bk, int splits)
@@ -128,16 +129,22 @@ inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, i
 {
     if (dtype != kF16 && dtype != kBF16) return kErrUnsupportedDtype;
     if (out_dtype != kF32 && out_dtype != dtype) return kErrUnsupportedDtype;
-    const int64_t lim = (int64_t(1) << 31) - 1;
+    // Tile and panel coordinates are 32-bit TMA coordinates: rounded up to a
+    // whole tile (at most 256) they must stay below 2^31.
+    const int64_t lim = kMaxDim;
     if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim) return kErrInvalidArg;
     if (stages < 1) return kErrInvalidArg;
     if ((K * dtype_bytes(dtype)) % 16 != 0) return kErrAlignment;
     if ((N * dtype_bytes(out_dtype)) % 16 != 0) return kErrAlignment;
     if (!tile_supported(bm, bn, bk, dtype_bytes(dtype), pair)) return kErrNoKernel;
     if (splits < 1 || splits > kMaxSplits) return kErrInvalidArg;
+    // Split s writes its partial tile at workspace row s * ceil(M / bm) * bm + r,
+    // also a 32-bit TMA coordinate.
+    const int eff = effective_splits(K, bk, splits);
+    if (eff > 1 && int64_t(eff) * ((M + bm - 1) / bm) * bm > (int64_t(1) << 31) - 1) return kErrInvalidArg;
     if (stages > 64) return kErrSmemBudget;  // keeps the layout arithmetic in 32 bits
     // A split-K kernel stages fp32 partial tiles whatever the final output type.
-    const int staged = effective_splits(K, bk, splits) > 1 ? kF32 : out_dtype;
+    const int staged = eff > 1 ? kF32 : out_dtype;
     Layout L = make_layout(bm, bn, bk, stages, dtype, staged, pair);
     if (L.bound > smem_limit || int64_t(L.total) > smem_limit) return kErrSmemBudget;
     return kOk;

@@ -735,6 +735,17 @@ static int allow_max_smem(int dev, int limit)
     return kOk;
 }
 
+// Ranges of the plan options (NULL: all defaults).
+static int check_opts(const tgemm_plan_opts *opts, int num_stages)
+{
+    if (!opts) return kOk;
+    if (opts->cta_pair != 0 && opts->cta_pair != 1) return kErrInvalidArg;
+    if (opts->group_m < 0 || opts->group_m > 4096) return kErrInvalidArg;
+    if (opts->split_k < 0 || opts->split_k > kMaxSplits) return kErrInvalidArg;
+    if (opts->prefetch < 0 || opts->prefetch > num_stages) return kErrInvalidArg;
+    return kOk;
+}
+
 static unsigned long long env_watchdog()
 {
     const char *e = std::getenv("TGEMM_WATCHDOG_NS");
@@ -787,6 +798,8 @@ int tgemm_validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, in
 int tgemm_validate_ex(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N,
                       int block_K, int num_stages, int64_t smem_limit, const tgemm_plan_opts *opts)
 {
+    const int rc = check_opts(opts, num_stages);
+    if (rc != kOk) return rc;
     return validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit,
                     opts ? opts->cta_pair : 0, opts && opts->split_k > 1 ? opts->split_k : 1);
 }
@@ -803,10 +816,7 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     if (!out) return kErrInvalidArg;
     *out = nullptr;
     const int pair = opts && opts->cta_pair ? 1 : 0;
-    if (opts && (opts->cta_pair != 0 && opts->cta_pair != 1)) return kErrInvalidArg;
-    if (opts && (opts->group_m < 0 || opts->group_m > 4096)) return kErrInvalidArg;
-    if (opts && (opts->split_k < 0 || opts->split_k > kMaxSplits)) return kErrInvalidArg;
-    if (opts && (opts->prefetch < 0 || opts->prefetch > num_stages)) return kErrInvalidArg;
+    if (check_opts(opts, num_stages) != kOk) return kErrInvalidArg;
     const int splits = effective_splits(K, block_K, opts && opts->split_k > 1 ? opts->split_k : 1);
     // Argument checks that need no device come first.
     int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX, pair, splits);

@@ -92,6 +92,14 @@ def test_validate_rules(lib):
     assert V(-1, 128, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
     assert V(128, 128, -8, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
     assert V(2 ** 31, 128, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
+    # tile-rounded coordinates must stay 32-bit: 2^31 - 257 is the largest M, N or K
+    big = 2 ** 31 - 257
+    assert V(big - 7, 128, 128, tg.F16, tg.F32, 256, 128, 32, 3, L) == tg.OK
+    assert V(big + 7, 128, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
+    assert V(128, big - 3, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.OK
+    assert V(128, big + 5, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
+    assert V(128, 128, big - 7, tg.F16, tg.F32, 128, 128, 128, 3, L) == tg.OK
+    assert V(128, 128, big + 9, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 0, L) == tg.ERR_INVALID_ARG
     # empty products and the empty reduction are valid
     assert V(0, 128, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.OK
@@ -113,6 +121,30 @@ def test_validate_rules(lib):
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 12, L) == tg.OK
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 14, L) == tg.ERR_SMEM_BUDGET
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 10 ** 6, L) == tg.ERR_SMEM_BUDGET
+
+
+def test_validate_ex_options(lib):
+    V = tg.tgemm_validate_ex
+    L = LIMIT_227K
+    # CTA pairs need 256-row tiles; each CTA of the pair is a block for the budget
+    assert V(4096, 4096, 4096, tg.F16, tg.F16, 256, 224, 128, 3, L, cta_pair=1) == tg.OK
+    assert V(4096, 4096, 4096, tg.F16, tg.F16, 128, 224, 64, 3, L, cta_pair=1) == tg.ERR_NO_KERNEL
+    # split-K: at most 64 splits, and fp32 partial staging counts against the budget
+    assert V(512, 512, 32768, tg.F16, tg.F32, 256, 256, 128, 3, L, cta_pair=1, split_k=19) == tg.OK
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 128, 64, 4, L, split_k=65) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 128, 64, 4, L, split_k=-1) == tg.ERR_INVALID_ARG
+    # the workspace row of split s (s * ceil(M / bm) * bm + r) must stay a 32-bit coordinate
+    M = 2 ** 26
+    assert V(M, 4, 64 * 32, tg.F16, tg.F32, 128, 32, 32, 4, L, split_k=31) == tg.OK      # 31 * 2^26 < 2^31
+    assert V(M, 4, 64 * 32, tg.F16, tg.F32, 128, 32, 32, 4, L, split_k=32) == tg.ERR_INVALID_ARG
+    # option ranges, as tgemm_plan_ex checks them
+    assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, L, cta_pair=2) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, L, group_m=-1) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, L, group_m=4097) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, L, prefetch=5) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, L, prefetch=4) == tg.OK
+    # a split count above the number of k-blocks is cut down first, so it is not an error
+    assert V(M, 4, 2 * 32, tg.F16, tg.F32, 128, 32, 32, 4, L, split_k=64) == tg.OK
 
 
 def test_budget_rule_agrees_with_oracle_over_the_grid(lib):
