@@ -98,7 +98,8 @@ int tgemm_smem_limit(void);
  *   - dtype in {F16, BF16}, out_dtype in {F32, dtype}     -> UNSUPPORTED_DTYPE
  *   - M, N >= 0, K >= 0, each <= 2^31 - 257 (a coordinate
  *     rounded up to a whole tile stays a 32-bit TMA
- *     coordinate); num_stages >= 1                         -> INVALID_ARG
+ *     coordinate); num_stages >= 1; at most 2^30 output
+ *     tiles (times K splits)                               -> INVALID_ARG
  *   - K % 8 == 0, N * out_bytes % 16 == 0 (row pitch)      -> ALIGNMENT
  *   - block_M in {128, 256}; block_N a multiple of 32 in
  *     [32, 256]; block_K in {16, 32, 64, 128} (16-bit

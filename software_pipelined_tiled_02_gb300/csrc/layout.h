@@ -114,6 +114,7 @@ inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out
 // Largest number of K splits a plan accepts.
 constexpr int kMaxSplits = 64;
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1 - 256;  // largest M, N or K
+constexpr int64_t kMaxUnits = int64_t(1) << 30;             // largest tiles x splits
 
 // Effective number of K splits: at least one k-block per split.
 inline int effective_splits(int64_t K, int bk, int splits)
@@ -142,6 +143,9 @@ inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, i
     // also a 32-bit TMA coordinate.
     const int eff = effective_splits(K, bk, splits);
     if (eff > 1 && int64_t(eff) * ((M + bm - 1) / bm) * bm > (int64_t(1) << 31) - 1) return kErrInvalidArg;
+    // Work units (tiles x splits) are counted in 32-bit integers by the
+    // persistent schedule, with room for one more stride of CTAs.
+    if (((M + bm - 1) / bm) * ((N + bn - 1) / bn) * int64_t(eff) > kMaxUnits) return kErrInvalidArg;
     if (stages > 64) return kErrSmemBudget;  // keeps the layout arithmetic in 32 bits
     // A split-K kernel stages fp32 partial tiles whatever the final output type.
     const int staged = eff > 1 ? kF32 : out_dtype;

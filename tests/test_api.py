@@ -100,6 +100,9 @@ def test_validate_rules(lib):
     assert V(128, big + 5, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
     assert V(128, 128, big - 7, tg.F16, tg.F32, 128, 128, 128, 3, L) == tg.OK
     assert V(128, 128, big + 9, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.ERR_INVALID_ARG
+    # at most 2^30 output tiles: a 2^22 x 2^23 C in 128 x 32 tiles is 2^15 x 2^18 = 2^33 tiles
+    assert V(2 ** 22, 2 ** 23, 64, tg.F16, tg.F32, 128, 32, 32, 3, L) == tg.ERR_INVALID_ARG
+    assert V(2 ** 22, 2 ** 20, 64, tg.F16, tg.F32, 128, 32, 32, 3, L) == tg.OK  # 2^15 x 2^15 tiles
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 0, L) == tg.ERR_INVALID_ARG
     # empty products and the empty reduction are valid
     assert V(0, 128, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.OK
