@@ -735,6 +735,95 @@ static int allow_max_smem(int dev, int limit)
     return kOk;
 }
 
+// Kernel parameters of a launch configuration (everything but the tensor maps,
+// the status record and the watchdog).  pair: CTA pairs; splits: effective K
+// splits; prefetch: the producer's lead in k-blocks.
+static void fill_params(Params &q, const Layout &L, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
+                        int block_M, int block_N, int block_K, int num_stages, int pair, int splits, int prefetch,
+                        int group_m, int tiles_m, int tiles_n)
+{
+    std::memset(&q, 0, sizeof(q));
+    q.M = int(M);
+    q.N = int(N);
+    q.K = int(K);
+    q.num_kb = int((K + block_K - 1) / block_K);
+    q.tiles_m = tiles_m;
+    q.tiles_n = tiles_n;
+    q.num_tiles = tiles_m * tiles_n;
+    q.group_m = group_m;
+    q.splits = splits;
+    // effective_splits guarantees every split a non-empty k-block range
+    q.kb_per_split = splits > 1 ? (q.num_kb + splits - 1) / splits : q.num_kb;
+    q.prefetch = prefetch;
+    q.num_units = q.num_tiles * splits;
+    q.split_rows = tiles_m * block_M;
+    q.bm = block_M;
+    q.bn = block_N;
+    q.bk = block_K;
+    q.stages = num_stages;
+    q.n_kstep = block_K * L.in_bytes / 32;  // one MMA consumes K = 16 elements = 32 bytes
+    q.m_halves = L.m_halves;
+    q.a_rows = L.a_rows;
+    q.b_rows = L.b_rows;
+    // The kernel's own output: fp32 partials when K is split, else C's type.
+    q.out_mode = splits > 1 ? 0 : out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
+    q.acc_stages = L.acc_stages;
+    q.acc_cols = L.acc_cols;
+    q.tmem_cols = L.tmem_cols;
+    // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
+    // format (bits 7-9, 10-12: 0 fp16, 1 bf16), both K-major (bits 15, 16 =
+    // 0), N >> 3 (bits 17-22), M >> 4 (bits 24-28): M = 128 for one CTA,
+    // M = 256 for the CTA pair.
+    const uint32_t ab = dtype == kBF16 ? 1u : 0u;
+    const uint32_t mma_m = pair ? 256u : 128u;
+    q.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(block_N >> 3) << 17) | ((mma_m >> 4) << 24);
+    q.a_slot = round_up(L.a_stage_bytes, kSmemAlign);
+    q.b_slot = round_up(L.b_stage_bytes, kSmemAlign);
+    // Bytes that complete one full[s] phase: this CTA's boxes, or both CTAs' in pair mode.
+    q.stage_tx = (L.a_stage_bytes + L.b_stage_bytes) * (pair ? 2u : 1u);
+    q.row_bytes = uint32_t(L.swizzle_bytes);
+    q.panels = L.panels;
+    q.panel_k = L.swizzle_bytes / L.in_bytes;
+    q.a_panel16 = (uint32_t(L.a_rows) * uint32_t(L.swizzle_bytes)) >> 4;
+    q.b_panel16 = (uint32_t(L.b_rows) * uint32_t(L.swizzle_bytes)) >> 4;
+    q.off_a = L.off_a;
+    q.off_b = L.off_b;
+    q.off_c = L.off_c;
+    q.off_bar = L.off_bar;
+    q.c_buf_bytes = L.c_buf_bytes;
+    q.epi_bufs = L.epi_bufs;
+    // Leading byte offset is unused for swizzled K-major tiles whose K extent
+    // per MMA lies inside one swizzle row; encode 16 bytes.  Stride byte
+    // offset: 8 rows of one swizzle span each.
+    q.desc_lo_flags = (1u << 16);
+    const uint32_t sbo = 8u * uint32_t(L.swizzle_bytes);
+    q.desc_hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (desc_layout_for(L.swizzle_bytes) << 29);
+}
+
+// Tensor maps of A, B and the kernel's output: C, or with split K the
+// workspace `work`, viewed as [splits * split_rows, N] fp32.
+static int encode_maps(Params &q, const Layout &L, int dtype, int out_dtype, const void *A, const void *B, void *C,
+                       float *work)
+{
+    const uint64_t M = uint64_t(q.M), N = uint64_t(q.N), K = uint64_t(q.K);
+    int rc = kOk;
+    if (K > 0) {
+        const CUtensorMapSwizzle swz = swizzle_for(L.swizzle_bytes);
+        const uint32_t box_k = uint32_t(L.swizzle_bytes / L.in_bytes);  // one K-panel per box
+        const uint64_t pitch = K * uint64_t(L.in_bytes);
+        rc = encode_2d(&q.tmA, dtype, A, K, M, pitch, box_k, uint32_t(L.a_rows), swz, operand_promotion(pitch));
+        if (rc == kOk)
+            rc = encode_2d(&q.tmB, dtype, B, K, N, pitch, box_k, uint32_t(L.b_rows), swz, operand_promotion(pitch));
+    }
+    if (rc != kOk) return rc;
+    if (q.splits > 1)
+        return encode_2d(&q.tmC, kF32, work, N, uint64_t(q.splits) * uint64_t(q.split_rows), N * 4u,
+                         uint32_t(kEpiCols), 32u, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    return encode_2d(&q.tmC, out_dtype, C, N, M, N * uint64_t(L.out_bytes), uint32_t(kEpiCols), 32u,
+                     L.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE);
+}
+
 // Ranges of the plan options (NULL: all defaults).
 static int check_opts(const tgemm_plan_opts *opts, int num_stages)
 {
@@ -909,66 +998,10 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     }
 
     Params &q = p->params;
-    std::memset(&q, 0, sizeof(q));
-    const Layout &L = p->L;
-    q.M = int(M);
-    q.N = int(N);
-    q.K = int(K);
-    q.num_kb = int((K + block_K - 1) / block_K);
-    q.tiles_m = p->tiles_m;
-    q.tiles_n = p->tiles_n;
-    q.num_tiles = p->num_tiles;
-    q.group_m = p->group_m;
-    q.splits = splits;
-    // effective_splits guarantees every split a non-empty k-block range
-    q.kb_per_split = splits > 1 ? (q.num_kb + splits - 1) / splits : q.num_kb;
-    q.prefetch = opts && opts->prefetch > 0 ? opts->prefetch : num_stages;
-    q.num_units = p->num_tiles * splits;
-    q.split_rows = p->tiles_m * block_M;
-    q.bm = block_M;
-    q.bn = block_N;
-    q.bk = block_K;
-    q.stages = num_stages;
-    q.n_kstep = block_K * L.in_bytes / 32;  // one MMA consumes K = 16 elements = 32 bytes
-    q.m_halves = L.m_halves;
-    q.a_rows = L.a_rows;
-    q.b_rows = L.b_rows;
-    // The kernel's own output: fp32 partials when K is split, else C's type.
-    q.out_mode = splits > 1 ? 0 : out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
-    q.acc_stages = L.acc_stages;
-    q.acc_cols = L.acc_cols;
-    q.tmem_cols = L.tmem_cols;
-    // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
-    // format (bits 7-9, 10-12: 0 fp16, 1 bf16), both K-major (bits 15, 16 =
-    // 0), N >> 3 (bits 17-22), M >> 4 (bits 24-28): M = 128 for one CTA,
-    // M = 256 for the CTA pair.
-    const uint32_t ab = dtype == kBF16 ? 1u : 0u;
-    const uint32_t mma_m = pair ? 256u : 128u;
-    q.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(block_N >> 3) << 17) | ((mma_m >> 4) << 24);
-    q.a_slot = round_up(L.a_stage_bytes, kSmemAlign);
-    q.b_slot = round_up(L.b_stage_bytes, kSmemAlign);
-    // Bytes that complete one full[s] phase: this CTA's boxes, or both CTAs' in pair mode.
-    q.stage_tx = (L.a_stage_bytes + L.b_stage_bytes) * (pair ? 2u : 1u);
-    q.row_bytes = uint32_t(L.swizzle_bytes);
-    q.panels = L.panels;
-    q.panel_k = L.swizzle_bytes / L.in_bytes;
-    q.a_panel16 = (uint32_t(L.a_rows) * uint32_t(L.swizzle_bytes)) >> 4;
-    q.b_panel16 = (uint32_t(L.b_rows) * uint32_t(L.swizzle_bytes)) >> 4;
-    q.off_a = L.off_a;
-    q.off_b = L.off_b;
-    q.off_c = L.off_c;
-    q.off_bar = L.off_bar;
-    q.c_buf_bytes = L.c_buf_bytes;
-    q.epi_bufs = L.epi_bufs;
-    // Leading byte offset is unused for swizzled K-major tiles whose K extent
-    // per MMA lies inside one swizzle row; encode 16 bytes.  Stride byte
-    // offset: 8 rows of one swizzle span each.
-    q.desc_lo_flags = (1u << 16);
-    const uint32_t sbo = 8u * uint32_t(L.swizzle_bytes);
-    q.desc_hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (desc_layout_for(L.swizzle_bytes) << 29);
+    fill_params(q, p->L, M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, pair, splits,
+                opts && opts->prefetch > 0 ? opts->prefetch : num_stages, p->group_m, p->tiles_m, p->tiles_n);
     q.watchdog_ns = p->watchdog_ns;
     q.status = p->d_status;
-    q.debug_stall = 0;
     *out = p;
     return kOk;
 }
@@ -978,29 +1011,7 @@ static int aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr)
 static int prepare_maps(tgemm_plan_s *p, const void *A, const void *B, void *C)
 {
     if (p->maps_valid && p->cA == A && p->cB == B && p->cC == C) return kOk;
-    Params &q = p->params;
-    const Layout &L = p->L;
-    int rc = kOk;
-    if (p->K > 0) {
-        CUtensorMapSwizzle swz = swizzle_for(L.swizzle_bytes);
-        const uint32_t box_k = uint32_t(L.swizzle_bytes / L.in_bytes);  // one K-panel per box
-        rc = encode_2d(&q.tmA, p->dtype, A, uint64_t(p->K), uint64_t(p->M), uint64_t(p->K) * L.in_bytes, box_k,
-                       uint32_t(L.a_rows), swz, operand_promotion(uint64_t(p->K) * L.in_bytes));
-        if (rc == kOk)
-            rc = encode_2d(&q.tmB, p->dtype, B, uint64_t(p->K), uint64_t(p->N), uint64_t(p->K) * L.in_bytes, box_k,
-                           uint32_t(L.b_rows), swz, operand_promotion(uint64_t(p->K) * L.in_bytes));
-    }
-    if (rc == kOk) {
-        if (p->splits > 1)  // partial tiles go to the workspace, viewed as [splits * M, N] fp32
-            rc = encode_2d(&q.tmC, kF32, p->d_work, uint64_t(p->N), uint64_t(p->splits) * uint64_t(q.split_rows),
-                           uint64_t(p->N) * 4u, uint32_t(kEpiCols), 32u, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_NONE);
-        else
-            rc = encode_2d(&q.tmC, p->out_dtype, C, uint64_t(p->N), uint64_t(p->M), uint64_t(p->N) * L.out_bytes,
-                           uint32_t(kEpiCols), 32u,
-                           L.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                           CU_TENSOR_MAP_L2_PROMOTION_NONE);
-    }
+    const int rc = encode_maps(p->params, p->L, p->dtype, p->out_dtype, A, B, C, p->d_work);
     if (rc != kOk) {
         p->maps_valid = false;
         return rc;
@@ -1254,67 +1265,11 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     const int grid = tiles < sms ? tiles : sms;
 
     Params q;
-    std::memset(&q, 0, sizeof(q));
-    q.M = int(M);
-    q.N = int(N);
-    q.K = int(K);
-    q.num_kb = int((K + block_K - 1) / block_K);
-    q.tiles_m = tiles_m;
-    q.tiles_n = tiles_n;
-    q.num_tiles = tiles;
-    q.splits = 1;
-    q.kb_per_split = q.num_kb;
-    q.prefetch = num_stages;
-    q.num_units = tiles;
-    q.split_rows = tiles_m * block_M;
-    q.group_m = 8;
-    q.bm = block_M;
-    q.bn = block_N;
-    q.bk = block_K;
-    q.stages = num_stages;
-    q.n_kstep = block_K * L.in_bytes / 32;
-    q.m_halves = L.m_halves;
-    q.a_rows = L.a_rows;
-    q.b_rows = L.b_rows;
-    q.out_mode = out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
-    q.acc_stages = L.acc_stages;
-    q.acc_cols = L.acc_cols;
-    q.tmem_cols = L.tmem_cols;
-    const uint32_t ab = dtype == kBF16 ? 1u : 0u;
-    q.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(block_N >> 3) << 17) | (uint32_t(128 >> 4) << 24);
-    q.a_slot = round_up(L.a_stage_bytes, kSmemAlign);
-    q.b_slot = round_up(L.b_stage_bytes, kSmemAlign);
-    q.stage_tx = L.a_stage_bytes + L.b_stage_bytes;
-    q.row_bytes = uint32_t(L.swizzle_bytes);
-    q.panels = L.panels;
-    q.panel_k = L.swizzle_bytes / L.in_bytes;
-    q.a_panel16 = (uint32_t(L.a_rows) * uint32_t(L.swizzle_bytes)) >> 4;
-    q.b_panel16 = (uint32_t(L.b_rows) * uint32_t(L.swizzle_bytes)) >> 4;
-    q.off_a = L.off_a;
-    q.off_b = L.off_b;
-    q.off_c = L.off_c;
-    q.off_bar = L.off_bar;
-    q.c_buf_bytes = L.c_buf_bytes;
-    q.epi_bufs = L.epi_bufs;
-    q.desc_lo_flags = (1u << 16);
-    const uint32_t sbo = 8u * uint32_t(L.swizzle_bytes);
-    q.desc_hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (desc_layout_for(L.swizzle_bytes) << 29);
+    fill_params(q, L, M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, 0, 1, num_stages, 8,
+                tiles_m, tiles_n);
     q.watchdog_ns = env_watchdog();
     q.status = scratch;
-    q.debug_stall = 0;
-    if (K > 0) {
-        const CUtensorMapSwizzle swz = swizzle_for(L.swizzle_bytes);
-        const uint32_t box_k = uint32_t(L.swizzle_bytes / L.in_bytes);  // one K-panel per box
-        rc = encode_2d(&q.tmA, dtype, A, uint64_t(K), uint64_t(M), uint64_t(K) * L.in_bytes, box_k,
-                       uint32_t(L.a_rows), swz, operand_promotion(uint64_t(K) * L.in_bytes));
-        if (rc == kOk)
-            rc = encode_2d(&q.tmB, dtype, B, uint64_t(K), uint64_t(N), uint64_t(K) * L.in_bytes, box_k,
-                           uint32_t(L.b_rows), swz, operand_promotion(uint64_t(K) * L.in_bytes));
-    }
-    if (rc == kOk)
-        rc = encode_2d(&q.tmC, out_dtype, C, uint64_t(N), uint64_t(M), uint64_t(N) * L.out_bytes,
-                       uint32_t(kEpiCols), 32u, L.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                       CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    rc = encode_maps(q, L, dtype, out_dtype, A, B, C, nullptr);
     if (rc != kOk) return rc;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
