@@ -41,6 +41,48 @@ def test_library_exports_every_declared_function(lib):
     assert sorted(tg.SYMBOLS) == declared
 
 
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "tgemm.h"
+
+int main(void)
+{
+    tgemm_plan_opts opts = {1, 2, 1, 0};  /* cta_pair, group_m, split_k, prefetch */
+    int64_t bound = tgemm_smem_bound(TGEMM_F16, 128, 128, 32, 3);
+    int one = tgemm_validate(4096, 4096, 4096, TGEMM_F16, TGEMM_F16, 256, 224, 64, 3, 232448);
+    int pair = tgemm_validate_ex(4096, 4096, 4096, TGEMM_F16, TGEMM_F16, 256, 224, 128, 3, 232448, &opts);
+    int over = tgemm_validate(4000, 3000, 5000, TGEMM_F16, TGEMM_F32, 256, 256, 64, 4, 232448);
+    const char *msg = tgemm_strerror(TGEMM_ERR_SMEM_BUDGET);
+    printf("%lld %d %d %d %s\n", (long long)bound, one, pair, over, msg);
+    return bound == 3 * (128 * 32 + 32 * 128) * 2 && one == TGEMM_OK && pair == TGEMM_OK &&
+                   over == TGEMM_ERR_SMEM_BUDGET && strlen(msg) > 0
+               ? 0
+               : 1;
+}
+"""
+
+
+def test_header_is_c_and_links(lib, tmp_path):
+    """The public header compiles as strict C99 and a C program links and calls the library."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(tg.LIB_PATH)
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+           str(src), "-L", libdir, "-ltgemm", "-Wl,-rpath," + libdir, "-o", str(exe)]
+    out = subprocess.run(cmd, capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0, run.stdout + run.stderr
+
+
 def test_strerror_covers_every_code(lib):
     texts = {tg.strerror(c) for c in range(9)}
     assert len(texts) == 9
