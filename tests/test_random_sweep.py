@@ -2,7 +2,7 @@
 
 Each case draws operand and output dtypes, a ragged shape (the only
 constraint is the 16-byte row-pitch rule), a tile, a depth the shared memory
-admits, CTA pairs, a K split and a producer lead.  It then compares the
+admits, CTA pairs, a K split, a producer lead and a raster group.  It then compares the
 kernel's C with the fp64 oracle element by element, to the tolerance of
 oracle.check.  The draws come from one fixed seed, so a failure names a
 reproducible case.
@@ -24,10 +24,11 @@ SINGLE_TILES = [(128, 128, 32), (128, 256, 64), (256, 128, 64), (128, 64, 16), (
                 (256, 96, 128), (128, 32, 64), (256, 256, 64), (128, 192, 64)]
 PAIR_TILES = [(256, 256, 128), (256, 224, 128), (256, 256, 64), (256, 128, 32), (256, 64, 16), (256, 32, 64),
               (256, 192, 128), (256, 160, 64)]
-N_CASES = int(os.environ.get("TGEMM_SWEEP_CASES", "160"))  # more for a longer soak
+N_CASES = int(os.environ.get("TGEMM_SWEEP_CASES", "400"))  # more for a longer soak
+SEED = int(os.environ.get("TGEMM_SWEEP_SEED", "20261202"))   # another seed draws other cases
 
 
-def draw_cases(tg, n=N_CASES, seed=20261202):
+def draw_cases(tg, n=N_CASES, seed=SEED):
     rng = np.random.default_rng(seed)
     limit = tg.tgemm_smem_limit()
     cases = []
@@ -46,16 +47,18 @@ def draw_cases(tg, n=N_CASES, seed=20261202):
                                 split_k=split) != tg.OK:
             continue
         prefetch = int(rng.integers(1, stages + 1)) if rng.random() < 0.25 else 0
-        cases.append((M, N, K, dtype, out, block, stages, pair, split, prefetch, int(rng.integers(1 << 30))))
+        group = int(rng.choice([0, 0, 1, 2, 3, 16]))
+        cases.append((M, N, K, dtype, out, block, stages, pair, split, prefetch, group, int(rng.integers(1 << 30))))
     return cases
 
 
 def test_random_sweep_matches_oracle(cuda_lib):
     tg = cuda_lib
     failures = []
-    for i, (M, N, K, dtype, out, block, stages, pair, split, prefetch, seed) in enumerate(draw_cases(tg)):
+    for i, (M, N, K, dtype, out, block, stages, pair, split, prefetch, group, seed) in enumerate(draw_cases(tg)):
         A, B = inputs.operands(seed, M, N, K, dtype, "normal")
-        plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair, split_k=split, prefetch=prefetch)
+        plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair, split_k=split, prefetch=prefetch,
+                       group_m=group)
         C = torch.full((M, N), float("nan"), dtype=TORCH[out], device="cuda")
         plan.run(inputs.bits_to_torch(A, dtype).cuda(), inputs.bits_to_torch(B, dtype).cuda(), C)
         torch.cuda.synchronize()
@@ -64,5 +67,5 @@ def test_random_sweep_matches_oracle(cuda_lib):
         R, S = oracle.gemm(A, B, dtype)
         ok, worst, idx = oracle.check(C.float().cpu().double().numpy(), R, S, out)
         if code != 0 or not ok:
-            failures.append((i, (M, N, K, dtype, out, block, stages, pair, split, prefetch, seed), code, worst))
+            failures.append((i, (M, N, K, dtype, out, block, stages, pair, split, prefetch, group, seed), code, worst))
     assert not failures, failures
