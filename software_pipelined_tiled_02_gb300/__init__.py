@@ -286,9 +286,22 @@ class Plan:
         return C
 
     def run_host(self, hA, hB, hC, dA, dB, dC, stream=None):
-        """Host operands in, host result out (copies enqueued by the library)."""
+        """Host operands in, host result out (copies enqueued by the library).
+
+        hA, hB, hC are CPU tensors (pinned for asynchronous copies), dA, dB, dC
+        the device buffers the library copies through; all contiguous, with
+        the plan's shapes and dtypes."""
         import torch
 
+        self._check(dA, dB, dC)
+        for name, h, d in (("hA", hA, dA), ("hB", hB, dB), ("hC", hC, dC)):
+            if h.is_cuda:
+                raise ValueError(f"{name} must be a host (CPU) tensor")
+            if h.dtype != d.dtype or tuple(h.shape) != tuple(d.shape):
+                raise ValueError(f"{name} must match its device buffer: {d.dtype} {tuple(d.shape)}, "
+                                 f"got {h.dtype} {tuple(h.shape)}")
+            if not h.is_contiguous():
+                raise ValueError(f"{name} must be contiguous (row-major)")
         s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
         rc = tgemm_run_host(self.handle, hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), dA.data_ptr(),
                             dB.data_ptr(), dC.data_ptr(), s)

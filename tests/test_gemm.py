@@ -374,4 +374,20 @@ def test_run_host_argument_errors(cuda_lib):
     x = torch.zeros(128 * 128, dtype=torch.float32, device="cuda").data_ptr()
     assert cuda_lib.tgemm_run_host(plan.handle, 0, 0, 0, x, x, x) == cuda_lib.ERR_INVALID_ARG
     assert cuda_lib.tgemm_run_host(None, 0, 0, 0, 0, 0, 0) == cuda_lib.ERR_INVALID_ARG
+    # the binding checks every buffer against the plan before the library copies anything
+    dA = torch.zeros(128, 64, dtype=torch.float16, device="cuda")
+    dB = torch.zeros(128, 64, dtype=torch.float16, device="cuda")
+    dC = torch.zeros(128, 128, dtype=torch.float32, device="cuda")
+    hA, hB, hC = dA.cpu(), dB.cpu(), dC.cpu()
+    with pytest.raises(ValueError):
+        plan.run_host(hA[:64], hB, hC, dA, dB, dC)           # host A too small
+    with pytest.raises(ValueError):
+        plan.run_host(hA, hB, hC.half(), dA, dB, dC)          # host C of the wrong dtype
+    with pytest.raises(ValueError):
+        plan.run_host(dA, hB, hC, dA, dB, dC)                 # a device tensor where host A belongs
+    with pytest.raises(ValueError):
+        plan.run_host(hA, hB, hC, dA, dB, dC[:64])            # device C too small
+    plan.run_host(hA, hB, hC, dA, dB, dC)
+    torch.cuda.synchronize()
+    assert plan.status()[0] == 0 and not hC.any()
     plan.close()
