@@ -102,7 +102,8 @@ int tgemm_smem_limit(void);
  *     tiles (times K splits)                               -> INVALID_ARG
  *   - K % 8 == 0, N * out_bytes % 16 == 0 (row pitch)      -> ALIGNMENT
  *   - block_M in {128, 256}; block_N a multiple of 32 in
- *     [32, 256]; block_K in {16, 32, 64, 128} (16-bit
+ *     [32, 256] (with cta_pair also 320, 384, 448, 512);
+ *     block_K in {16, 32, 64, 128} (16-bit
  *     operands: rows of 32, 64 or 128 bytes, or two 128-byte
  *     K-panels for 128)                                     -> NO_KERNEL
  *   - tgemm_smem_bound > smem_limit or
@@ -135,7 +136,11 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
  *     of CTAs (thread-block clusters of 2) on neighbouring SMs share each
  *     block_M = 256 tile: one M = 256 tensor-core instruction per K step spans
  *     both SMs, each CTA holds 128 rows of A, block_N / 2 rows of B and 128
- *     rows of the accumulator.  Only block_M = 256 is accepted.  Each CTA is a
+ *     rows of the accumulator.  Only block_M = 256 is accepted.  block_N may
+ *     then also be 320, 384, 448 or 512: two N = block_N / 2 instructions per K
+ *     step share the A operand (each SM pulls less operand data per FLOP, but
+ *     the accumulator fills tensor memory, so the epilogue of a tile no longer
+ *     overlaps the next tile's K loop).  Each CTA is a
  *     block in the sense of the pages' budget rule: the bound checked is
  *     num_stages x (128 x block_K + block_K x block_N / 2) x element size.
  *   group_m: M-tiles per raster group of the persistent schedule (0: 8).

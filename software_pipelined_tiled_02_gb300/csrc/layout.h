@@ -45,6 +45,7 @@ struct Layout {
     uint32_t total;          // bytes requested, including alignment slack
     int64_t bound;           // stages * (A tile + B tile): the budget rule's bound
     int m_halves;            // bm / 128 MMAs of M = 128 per k-step
+    int n_halves;            // pair tiles wider than one MMA (block_N > 256): two MMAs of N = block_N / 2
     int acc_cols;            // TMEM columns of one accumulator (m_halves * bn)
     int acc_stages;          // accumulators in flight (2 lets the epilogue overlap the next tile)
     int tmem_cols;           // power of two >= 32 allocated per CTA
@@ -60,12 +61,15 @@ inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 // 128-byte spans (block_K = 128 for 16-bit operands: the slot then holds two
 // K-panels of 64 elements, each a standard 128-byte-swizzled tile).  The
 // CTA-pair mode implements only block_M = 256 (one M = 256 MMA over the two
-// CTAs' 128-row halves).
+// CTAs' 128-row halves), and also tiles of 320 to 512 columns in steps of 64:
+// two MMAs of N = block_N / 2 per k-step that share the A operand, so each SM
+// pulls a quarter less operand data per FLOP than with 256 columns.
 inline bool tile_supported(int bm, int bn, int bk, int in_bytes, int pair = 0)
 {
     if (pair && bm != 256) return false;
     if (bm != 128 && bm != 256) return false;
-    if (bn < 32 || bn > 256 || bn % 32 != 0) return false;
+    const bool wide = pair && bn > 256 && bn <= 512 && bn % 64 == 0;
+    if (!wide && (bn < 32 || bn > 256 || bn % 32 != 0)) return false;
     int row = bk * in_bytes;
     return (row == 32 || row == 64 || row == 128 || row == 256) && bk > 0;
 }
@@ -99,6 +103,7 @@ inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out
     L.bar_bytes = barrier_block_bytes(stages);
     L.total = L.off_bar + L.bar_bytes + kSmemAlign;  // slack to align the dynamic base
     L.m_halves = pair ? 1 : bm / 128;
+    L.n_halves = pair && bn > 256 ? 2 : 1;
     L.acc_cols = L.m_halves * bn;
     L.acc_stages = (2 * L.acc_cols <= kTmemColsMax) ? 2 : 1;
     int need = L.acc_stages * L.acc_cols;

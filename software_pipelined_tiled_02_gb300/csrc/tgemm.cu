@@ -68,6 +68,12 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     int bm, bn, bk, stages;
     int n_kstep;                // bk / 16 MMAs along K per slot
     int m_halves;               // bm / 128 (1 in pair mode: one M = 256 MMA covers both CTAs)
+    int mma_per_kstep;          // MMAs per k-step: 2 M-halves (one CTA, bm = 256), 2 N-halves
+                                // (pair, bn > 256), else 1
+    uint32_t acc_step;          // TMEM columns between the accumulators of the two MMAs
+    uint32_t a_half16, b_half16; // descriptor offsets (16-byte units) of the second MMA's A and B
+    int n_halves;               // B boxes per K-panel: 2 for pair tiles wider than 256
+    int b_box_rows;             // rows of one B box (b_rows / n_halves)
     int a_rows, b_rows;         // operand rows this CTA loads per slot (pair: 128 and bn / 2)
     int out_mode;               // 0 fp32, 1 fp16, 2 bf16
     int acc_stages, acc_cols, tmem_cols;
@@ -199,11 +205,14 @@ struct MmaCtx {
 };
 
 // The MMA warp's main loop.  NK = MMAs of K = 16 per ring slot (block_K / 16),
-// MH = MMAs of M = 128 per k-step (block_M / 128; 1 in pair mode, where one
-// M = 256 MMA spans both CTAs).  Descriptors of slot s are the slot-0
-// descriptors plus s slot strides (address field in 16-byte units); k-step kk
-// adds 32 bytes, the second M-half adds 128 operand rows.  In pair mode this
-// runs in the even CTA only: its commits arrive on the barriers of both CTAs.
+// MH = MMAs per k-step: the two M = 128 halves of a one-CTA 256-row tile (the
+// second reads A 128 rows further on and writes the accumulator block_N
+// columns further on), or in pair mode the two N-halves of a tile wider than
+// 256 columns (the second reads the second half of this CTA's B rows and
+// writes block_N / 2 columns further on); 1 otherwise.  Descriptors of slot s
+// are the slot-0 descriptors plus s slot strides (address field in 16-byte
+// units); k-step kk adds 32 bytes.  In pair mode this runs in the even CTA
+// only: its commits arrive on the barriers of both CTAs.
 template <int NK, int MH, bool PAIR>
 __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volatile int *abort, int lane)
 {
@@ -226,7 +235,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
     };
     const uint64_t ad0 = smem_desc(c.sA, p), bd0 = smem_desc(c.sB, p);
     const uint64_t a_step = p.a_slot >> 4, b_step = p.b_slot >> 4;
-    const uint64_t a_half = (128u * p.row_bytes) >> 4;
+    const uint64_t a_half = p.a_half16, b_half = p.b_half16;
     const uint64_t a_panel = p.a_panel16, b_panel = p.b_panel16;
     int s = 0;
     uint32_t ph = 0;
@@ -242,7 +251,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
         if (!warp_wait(acc_empty(a), aph ^ 1u, p, abort, 1, it)) break;
         tc_fence_after();
         const uint32_t d = c.tmem + uint32_t(a * p.acc_cols);
-        const uint32_t d2 = d + uint32_t(p.bn);
+        const uint32_t d2 = d + p.acc_step;
         for (int kb = kb0; kb < kb1; ++kb) {
             if (!warp_wait(full(s), ph, p, abort, 1, it)) {
                 ok = false;
@@ -255,7 +264,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
                                                                   c.sA + uint32_t(S) * p.a_slot &&
                           uint32_t(bd & 0x3FFFu) << 4 >= c.sB &&
                           ((uint32_t(bd & 0x3FFFu) << 4) + p.b_slot) <= c.sB + uint32_t(S) * p.b_slot &&
-                          a * p.acc_cols + MH * p.bn <= p.tmem_cols && kb1 <= p.num_kb,
+                          (a + 1) * p.acc_cols <= p.tmem_cols && kb1 <= p.num_kb,
                       p, abort, 1, it);
             if (lane == 0 && in_range) {
                 const uint32_t first = kb != kb0 ? 1u : 0u;
@@ -266,7 +275,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
                     const uint64_t kb_ = uint64_t(2 * (kk & 3)) + uint64_t(kk >> 2) * b_panel;
 #pragma unroll
                     for (int h = 0; h < MH; ++h)
-                        mma(h ? d2 : d, ad + ka + (h ? a_half : 0), bd + kb_, kk == 0 ? first : 1u);
+                        mma(h ? d2 : d, ad + ka + (h ? a_half : 0), bd + kb_ + (h ? b_half : 0), kk == 0 ? first : 1u);
                 }
                 commit_both(empty(s));  // slot s (in both CTAs) may be refilled once these MMAs finish
             }
@@ -400,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         uint32_t phd = 0;
         for (int t = unit0; ok && t < p.num_units; t += ustride) {
             const Unit w = unit_coords(p, t);
-            const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn + int(rank) * p.b_rows;
+            const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn + int(rank) * p.b_box_rows;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 if (!warp_wait(empty(s), ph ^ 1u, p, abort, 0, issued)) {
                     ok = false;
@@ -429,7 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                         for (int pl = 0; pl < p.panels; ++pl) {
                             const int x = kb * p.bk + pl * p.panel_k;
                             tma_load_2d_pair(a_dst + (uint32_t(pl) * p.a_panel16 << 4), &p.tmA, x, m0, fb);
-                            tma_load_2d_pair(b_dst + (uint32_t(pl) * p.b_panel16 << 4), &p.tmB, x, n0, fb);
+                            // one B box per N-half: this CTA's rows of each half (N offset block_N / 2)
+                            for (int hb = 0; hb < p.n_halves; ++hb)
+                                tma_load_2d_pair(b_dst + ((uint32_t(pl) * p.b_panel16 + uint32_t(hb) * p.b_half16) << 4),
+                                                 &p.tmB, x, n0 + hb * (p.bn >> 1), fb);
                         }
                     } else {
                         mbar_arrive_expect_tx(full(s), p.stage_tx);
@@ -466,11 +478,11 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         __syncwarp();
     } else if (warp == 1) {
         // ---------------- MMA issuer: the warp runs the loop, lane 0 drives the tensor core.
-        // The k-steps per slot and the M-halves per tile are compile-time in
+        // The k-steps per slot and the MMAs per k-step are compile-time in
         // the issue loop, so each MMA costs one descriptor add.
         if (!PAIR || rank == 0) {
             const MmaCtx c{sA, sB, tmem, bars, S, stall, drain, unit0, ustride};
-            if (p.m_halves == 2)
+            if (p.mma_per_kstep == 2)
                 mma_dispatch_nk<2, PAIR>(p, c, abort, lane);
             else
                 mma_dispatch_nk<1, PAIR>(p, c, abort, lane);
@@ -765,6 +777,15 @@ static void fill_params(Params &q, const Layout &L, int64_t M, int64_t N, int64_
     q.m_halves = L.m_halves;
     q.a_rows = L.a_rows;
     q.b_rows = L.b_rows;
+    q.n_halves = L.n_halves;
+    q.b_box_rows = L.b_rows / L.n_halves;
+    q.mma_per_kstep = L.m_halves * L.n_halves;
+    // second MMA of a k-step: the lower M-half (128 rows of A further on, block_N
+    // accumulator columns further on) or the right N-half (the second group of this
+    // CTA's B rows, block_N / 2 columns further on)
+    q.acc_step = L.n_halves == 2 ? uint32_t(block_N / 2) : uint32_t(block_N);
+    q.a_half16 = L.m_halves == 2 ? (128u * uint32_t(L.swizzle_bytes)) >> 4 : 0u;
+    q.b_half16 = L.n_halves == 2 ? (uint32_t(q.b_box_rows) * uint32_t(L.swizzle_bytes)) >> 4 : 0u;
     // The kernel's own output: fp32 partials when K is split, else C's type.
     q.out_mode = splits > 1 ? 0 : out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
     q.acc_stages = L.acc_stages;
@@ -776,7 +797,8 @@ static void fill_params(Params &q, const Layout &L, int64_t M, int64_t N, int64_
     // M = 256 for the CTA pair.
     const uint32_t ab = dtype == kBF16 ? 1u : 0u;
     const uint32_t mma_m = pair ? 256u : 128u;
-    q.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(block_N >> 3) << 17) | ((mma_m >> 4) << 24);
+    const uint32_t mma_n = uint32_t(block_N / L.n_halves);
+    q.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((mma_n >> 3) << 17) | ((mma_m >> 4) << 24);
     q.a_slot = round_up(L.a_stage_bytes, kSmemAlign);
     q.b_slot = round_up(L.b_stage_bytes, kSmemAlign);
     // Bytes that complete one full[s] phase: this CTA's boxes, or both CTAs' in pair mode.
@@ -813,7 +835,8 @@ static int encode_maps(Params &q, const Layout &L, int dtype, int out_dtype, con
         const uint64_t pitch = K * uint64_t(L.in_bytes);
         rc = encode_2d(&q.tmA, dtype, A, K, M, pitch, box_k, uint32_t(L.a_rows), swz, operand_promotion(pitch));
         if (rc == kOk)
-            rc = encode_2d(&q.tmB, dtype, B, K, N, pitch, box_k, uint32_t(L.b_rows), swz, operand_promotion(pitch));
+            rc = encode_2d(&q.tmB, dtype, B, K, N, pitch, box_k, uint32_t(L.b_rows / L.n_halves), swz,
+                           operand_promotion(pitch));
     }
     if (rc != kOk) return rc;
     if (q.splits > 1)

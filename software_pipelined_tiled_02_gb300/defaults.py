@@ -19,7 +19,7 @@ from __future__ import annotations
 FROZEN = {
     (4096, 4096, 4096, 0, 0): ((256, 224, 128), 3, True, 1, 2),  # 1643 vs 1607 for one CTA 256x224x64, group 8
     (8192, 8192, 8192, 1, 1): ((256, 256, 128), 3, True),       # 1753 vs 1692 for one CTA 256x256x64
-    (4000, 3000, 5000, 0, 2): ((256, 224, 64), 6, True),        # 96.9 vs 99.0 us at S=5; 988 TF/s one CTA 256x192x64
+    (4000, 3000, 5000, 0, 2): ((256, 384, 64), 4, True),        # 94.0 vs 100.1 us for 256x224x64 S6 (96.9 vs 99.0 at S5)
     (512, 512, 32768, 0, 2): ((256, 256, 128), 3, True, 19),    # 514 vs 485 for 128x128x64 S6 split 9; 107 unsplit
     (128, 128, 128, 0, 2): ((128, 128, 32), 3),
 }
@@ -29,6 +29,7 @@ FROZEN = {
 # pair computes one 256-row tile on two SMs.
 CANDIDATES = (
     ((256, 256, 128), 3, 1.04, True),
+    ((256, 384, 64), 4, 1.04, True),   # two N = 192 MMAs per k-step; measured on 4000x3000x5000
     ((256, 224, 64), 5, 1.00, True),
     ((256, 256, 64), 3, 1.00, False),
     ((256, 224, 64), 3, 0.98, False),

@@ -95,6 +95,8 @@ def test_integer_inputs_bit_exact(cuda_lib, block, stages, dtype):
 # ------------------------------------------------------------ CTA-pair mode
 
 PAIR_CONFIGS = [
+    ((256, 512, 64), 4),     # two N = 256 MMAs per k-step sharing A
+    ((256, 384, 128), 2),    # two N = 192 MMAs, two K-panels per slot
     ((256, 256, 128), 3),
     ((256, 224, 128), 3),
     ((256, 256, 64), 4),
