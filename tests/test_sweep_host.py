@@ -72,3 +72,24 @@ def test_gb300_space_has_pairs_only_for_256_rows():
     key = lambda c: (c["block_M"], c["block_N"], c["block_K"], c["num_stages"], c["cta_pair"])  # noqa: E731
     ok = {key(c) for c in legal}
     assert (256, 256, 64, 6, 1) in ok and (256, 256, 64, 6, 0) not in ok and (256, 256, 64, 3, 0) in ok
+
+
+def test_frozen_defaults_are_legal_and_chosen():
+    from software_pipelined_tiled_02_gb300 import defaults
+
+    for (M, N, K, dt, od), entry in defaults.FROZEN.items():
+        cfg = defaults.choose(M, N, K, dt, od)
+        assert cfg["block"] == entry[0] and cfg["num_stages"] == entry[1]
+        rc = tg.tgemm_validate_ex(M, N, K, dt, od, *cfg["block"], cfg["num_stages"], 232448,
+                                  cta_pair=int(cfg["cta_pair"]), split_k=cfg["split_k"], group_m=cfg["group_m"])
+        assert rc == tg.OK, ((M, N, K), cfg, tg.strerror(rc))
+
+
+def test_wide_pair_tiles_only_in_pair_mode():
+    cfgs = sweep.enumerate_space(sweep.GB300_SPACE)
+    legal, rej = sweep.prune(cfgs, 8192, 8192, 8192, tg.BF16, tg.BF16, LIMIT, divisible=False)
+    key = lambda c: (c["block_M"], c["block_N"], c["block_K"], c["num_stages"], c["cta_pair"])  # noqa: E731
+    ok = {key(c) for c in legal}
+    no_kernel = {key(c) for c in rej["no_kernel"]}
+    assert (256, 512, 64, 4, 1) in ok and (256, 512, 64, 5, 1) not in ok   # 48 KB slots: four fit
+    assert (256, 512, 64, 2, 0) in no_kernel and (128, 384, 64, 2, 0) in no_kernel
