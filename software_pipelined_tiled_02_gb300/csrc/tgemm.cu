@@ -438,10 +438,11 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                         for (int pl = 0; pl < p.panels; ++pl) {
                             const int x = kb * p.bk + pl * p.panel_k;
                             tma_load_2d_pair(a_dst + (uint32_t(pl) * p.a_panel16 << 4), &p.tmA, x, m0, fb);
-                            // one B box per N-half: this CTA's rows of each half (N offset block_N / 2)
-                            for (int hb = 0; hb < p.n_halves; ++hb)
-                                tma_load_2d_pair(b_dst + ((uint32_t(pl) * p.b_panel16 + uint32_t(hb) * p.b_half16) << 4),
-                                                 &p.tmB, x, n0 + hb * (p.bn >> 1), fb);
+                            tma_load_2d_pair(b_dst + (uint32_t(pl) * p.b_panel16 << 4), &p.tmB, x, n0, fb);
+                            // a wide tile's second N-half: this CTA's rows of it, block_N / 2 further on
+                            if (p.n_halves == 2)
+                                tma_load_2d_pair(b_dst + ((uint32_t(pl) * p.b_panel16 + p.b_half16) << 4), &p.tmB, x,
+                                                 n0 + (p.bn >> 1), fb);
                         }
                     } else {
                         mbar_arrive_expect_tx(full(s), p.stage_tx);
