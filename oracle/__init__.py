@@ -186,12 +186,16 @@ def num_threads() -> int:
 
 
 def ulp(values, dtype: str) -> np.ndarray:
-    """Spacing of ``dtype`` numbers at each value's magnitude (float64)."""
+    """Spacing of ``dtype`` numbers at each value's magnitude (float64).
+
+    IEEE 754: with p significand bits and minimum normal exponent emin, the
+    spacing for |x| in [2^e, 2^(e+1)) is 2^(e - p + 1) when e >= emin; below
+    2^emin (subnormals, and zero) it is the subnormal step 2^(emin - p + 1).
+    """
     p, emin = {"f16": (11, -14), "bf16": (8, -126), "f32": (24, -126)}[dtype]
     a = np.abs(np.asarray(values, dtype=np.float64))
-    with np.errstate(divide="ignore"):
-        _, e = np.frexp(a)
-    e = np.maximum(e - 1, emin)
+    _, e = np.frexp(a)  # a = f * 2^e with f in [0.5, 1): |x| lies in [2^(e-1), 2^e)
+    e = np.where(a == 0, emin, np.maximum(e - 1, emin))
     return np.ldexp(1.0, e - (p - 1))
 
 

@@ -6,6 +6,10 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+# The mutation test runs the oracle pins against a deliberately broken copy of
+# the oracle package placed in another directory; that directory comes first.
+if os.environ.get("ORACLE_PKG_ROOT"):
+    sys.path.insert(0, os.environ["ORACLE_PKG_ROOT"])
 
 GOLDEN = os.path.join(ROOT, "tests", "golden")
 

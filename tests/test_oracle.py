@@ -264,3 +264,93 @@ def test_check_accepts_within_and_rejects_outside():
     assert not ok
     ok, _, _ = oracle.check(np.array([np.nan]), np.array([1.0]), np.array([1.0]), "f32")
     assert not ok
+
+
+def test_check_pages_leg_alone_rejects():
+    # A huge error scale S makes the target's bound 1e-4*S + 1e-5 loose; the
+    # pages' own check (rtol = atol = 1e-2 against torch.matmul) must still
+    # reject an output that is 0.5 away from a zero reference.
+    R, S = np.array([0.0]), np.array([1e4])
+    ok, worst, _ = oracle.check(np.array([0.5]), R, S, "f32")
+    assert not ok and worst == pytest.approx(0.5 / 1e-2)
+    # Its absolute part is 1e-2: 0.009 passes, 0.011 fails.
+    assert oracle.check(np.array([0.009]), R, S, "f32")[0]
+    assert not oracle.check(np.array([0.011]), R, S, "f32")[0]
+    # Its relative part is 1e-2 * |R|: at R = 100 an error of 1.0 passes
+    # (bound 1.01) and 1.02 fails.
+    R, S = np.array([100.0]), np.array([1e8])
+    assert oracle.check(R + 1.0, R, S, "f32")[0]
+    assert not oracle.check(R + 1.02, R, S, "f32")[0]
+    assert not oracle.check(-R, R, S, "bf16")[0]
+
+
+def test_check_bf16_output_allows_one_bf16_ulp():
+    # bfloat16 keeps 8 significand bits: its spacing at 1.0 is 2^-7.
+    R, S = np.array([1.0]), np.array([0.0])
+    assert oracle.check(np.array([1.0 + 2.0 ** -7]), R, S, "bf16")[0]
+    assert not oracle.check(np.array([1.0 + 2.0 ** -6]), R, S, "bf16")[0]
+    assert oracle.check(np.array([3.0 + 2.0 ** -6]), np.array([3.0]), S, "bf16")[0]
+    assert not oracle.check(np.array([3.0 + 2.0 ** -5]), np.array([3.0]), S, "bf16")[0]
+
+
+def test_check_f32_output_gets_no_ulp():
+    # The raw fp32 accumulator is compared with 1e-4*S + 1e-5 alone: at
+    # R = 2^20 (binary32 spacing 2^-3) an error of one fp32 ulp is rejected
+    # when S = 0, although the pages' relative bound (about 1e4) is far away.
+    R, S = np.array([2.0 ** 20]), np.array([0.0])
+    assert not oracle.check(R + 2.0 ** -3, R, S, "f32")[0]
+
+
+def test_check_rejects_infinities_against_finite():
+    R, S = np.array([1.0, 1.0]), np.array([1.0, 1.0])
+    assert not oracle.check(np.array([np.inf, 1.0]), R, S, "f32")[0]
+    assert not oracle.check(np.array([1.0, -np.inf]), R, S, "f16")[0]
+
+
+# -------------------------------------------------- output spacing (ulp)
+
+# IEEE 754 fixes each format's spacing.  binary16: p = 11 significand bits,
+# emin = -14.  bfloat16: p = 8, with binary32's exponent range (emin = -126).
+# binary32: p = 24, emin = -126.  For |x| in [2^e, 2^(e+1)) with e >= emin the
+# spacing is 2^(e - p + 1); below 2^emin (subnormals and zero) it is the
+# subnormal step 2^(emin - p + 1).
+ULP_FIXED = [
+    ("f16", 1.0, 2.0 ** -10), ("f16", 1.5, 2.0 ** -10), ("f16", -3.0, 2.0 ** -9), ("f16", 65504.0, 32.0),
+    ("f16", 2.0 ** -14, 2.0 ** -24), ("f16", 2.0 ** -20, 2.0 ** -24), ("f16", 0.0, 2.0 ** -24),
+    ("bf16", 1.0, 2.0 ** -7), ("bf16", 3.0, 2.0 ** -6), ("bf16", -0.75, 2.0 ** -8),
+    ("bf16", 2.0 ** -126, 2.0 ** -133), ("bf16", 2.0 ** -130, 2.0 ** -133), ("bf16", 0.0, 2.0 ** -133),
+    ("bf16", 2.0 ** 127, 2.0 ** 120),
+    ("f32", 1.0, 2.0 ** -23), ("f32", 3.0, 2.0 ** -22), ("f32", 2.0 ** -126, 2.0 ** -149),
+    ("f32", 1e-40, 2.0 ** -149), ("f32", 0.0, 2.0 ** -149), ("f32", 2.0 ** 127, 2.0 ** 104),
+]
+
+
+@pytest.mark.parametrize("fmt,x,want", ULP_FIXED, ids=lambda v: str(v))
+def test_ulp_fixed_values(fmt, x, want):
+    assert oracle.ulp(np.array([x]), fmt)[0] == want
+
+
+def test_ulp_matches_numpy_spacing_f16_f32():
+    # numpy's nextafter-based spacing of float16 / float32 numbers, across
+    # normal and subnormal magnitudes of both signs.
+    rng = np.random.default_rng(11)
+    for fmt, npt, lo, hi in (("f16", np.float16, -30, 15), ("f32", np.float32, -160, 127)):
+        mags = np.ldexp(rng.uniform(1.0, 2.0, 4000), rng.integers(lo, hi, 4000))
+        x = (mags * rng.choice([-1.0, 1.0], 4000)).astype(npt)
+        x = x[np.isfinite(x) & (x != 0)]
+        with np.errstate(over="ignore"):
+            want = np.spacing(np.abs(x)).astype(np.float64)  # gap above |x|
+        x, want = x[np.isfinite(want)], want[np.isfinite(want)]  # the largest finite value has no upper neighbour
+        assert np.array_equal(oracle.ulp(x.astype(np.float64), fmt), want)
+
+
+def test_ulp_matches_bf16_neighbours_from_bits():
+    # bfloat16 is the upper half of binary32: the value of pattern b is the
+    # float32 with bits b << 16, and its spacing is value(b + 1) - value(b).
+    rng = np.random.default_rng(12)
+    b = rng.integers(0x0001, 0x7F7F, 20000).astype(np.uint32)  # positive finite, below the largest
+    b = np.concatenate([b, np.array([0x0001, 0x007F, 0x0080, 0x3F80, 0x7F7E], np.uint32)])
+    val = (b << 16).view(np.float32).astype(np.float64)
+    nxt = ((b + 1) << 16).view(np.float32).astype(np.float64)
+    assert np.array_equal(oracle.ulp(val, "bf16"), nxt - val)
+    assert np.array_equal(oracle.ulp(-val, "bf16"), nxt - val)
