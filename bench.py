@@ -60,6 +60,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    ap.add_argument("--sustain-seconds", type=float, default=1.5,
+                    help="length of the sustained leg reported beside the timed steps (0: skip)")
     return ap.parse_args(argv)
 
 
@@ -190,7 +192,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -215,7 +217,8 @@ class ClockSampler:
             self.proc.kill()
         return self.summary()
 
-    def summary(self):
+    def summary(self, windows=None):
+        windows = self.windows if windows is None else windows
         rows = []
         for t, line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -228,7 +231,7 @@ class ClockSampler:
                 continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        inside = [r for r in rows if any(a - 0.15 <= r["t"] <= b + 0.15 for a, b in self.windows)]
+        inside = [r for r in rows if any(a - 0.05 <= r["t"] <= b + 0.05 for a, b in windows)]
         use = inside or rows
         reasons = set()
         for r in use:
@@ -302,6 +305,34 @@ def run_reference(args, w, world, rank):
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def sustained_leg(plan, dA, dB, dC, flush, stream, dev, seconds, flops, sampler):
+    """Flushed steps back to back for at least `seconds` of wall time; each
+    step's kernel is bracketed by CUDA events on the launching stream."""
+    import torch
+
+    batch = 256
+    t0 = time.time()
+    times = []
+    while True:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(batch)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            plan.run(dA, dB, dC, stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        times += [a.elapsed_time(b) for a, b in ev]
+        if time.time() - t0 >= seconds:
+            break
+    t1 = time.time()
+    if sampler:
+        sampler.mark(t0, t1)
+    mean = sum(times) / len(times)
+    return {"value": flops / (mean / 1e3) / 1e12, "unit": "TFLOP/s", "steps": len(times),
+            "seconds": t1 - t0, "ms_per_step": mean, "kernel_ms_median": statistics.median(times),
+            "_window": (t0, t1)}
+
+
 def config_block(args, w, block, stages):
     cfg = {"workload": args.workload, "M": w["M"], "N": w["N"], "K": w["K"], "operand_dtype": w["dtype"],
            "accumulate": "f32", "out_dtype": w["out"], "distribution": w["dist"], "seed": w["seed"],
@@ -353,13 +384,12 @@ def run_ours(args, w, world, rank, local):
     sampler = None if args.no_clocks else ClockSampler(local)
     if sampler:
         sampler.start()
+        time.sleep(0.4)  # let the sampler start; the warm-up below then runs right before the timed region
 
     for _ in range(args.warmup):
         flush.zero_()
         plan.run(dA, dB, dC, stream)
     torch.cuda.synchronize(dev)
-    if sampler:
-        time.sleep(0.4)  # let the sampler start before the timed region
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if dist:
@@ -384,6 +414,16 @@ def run_ours(args, w, world, rank, local):
     mean_ms = sum(kernel_ms) / len(kernel_ms)
     (max_mean_ms,) = reduce_max([mean_ms], dist, dev)
     value = aggregate(flops, max_mean_ms / 1e3, world)
+
+    # Sustained leg, reported beside `value` (never replacing it): the same
+    # flushed steps back to back for at least `--sustain-seconds`, long enough
+    # for the clock sampler to see the GPU under this load.
+    sustained = None
+    if args.sustain_seconds > 0:
+        sustained = sustained_leg(plan, dA, dB, dC, flush, stream, dev, args.sustain_seconds, flops, sampler)
+        code, detail = plan.status()
+        if code != tg.OK:
+            raise RuntimeError(f"kernel reported {tg.strerror(code)} {detail} in the sustained leg")
 
     e2e = None
     if not args.no_e2e:
@@ -434,6 +474,16 @@ def run_ours(args, w, world, rank, local):
         plans[1].close()
 
     clocks = sampler.stop() if sampler else None
+    if clocks:
+        clocks["windows"] = "timed steps, the sustained leg and the e2e leg (samples every 50 ms)"
+    if sustained is not None and sampler is not None:
+        sustained["clocks"] = sampler.summary(windows=[sustained.pop("_window")])
+        mhz = sustained["clocks"].get("sm_mhz")
+        if mhz:
+            # time x clock: kernel cycles per step, comparable across clock levels
+            sustained["mcycles_per_step"] = sustained["ms_per_step"] * mhz / 1e3
+    elif sustained is not None:
+        sustained.pop("_window", None)
 
     algo_bytes = (M * K + N * K) * 2 + M * N * (4 if w["out"] == "f32" else 2)
     roofline = roofline_for(flops, algo_bytes, mean_ms / 1e3, measured_peaks())
@@ -455,6 +505,7 @@ def run_ours(args, w, world, rank, local):
                                split_k=int(info["split_k"]), group_m=int(group_m) or 8), "roofline": roofline,
                 "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": args.steps * (2 if info["split_k"] > 1 else 1), "clocks": clocks,
+                "sustained": sustained,
                 "plan": {k: info[k] for k in ("grid", "num_tiles", "smem_bytes", "tmem_columns", "acc_stages")},
                 "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms), "max": max(kernel_ms)}}
     plan.close()

@@ -263,21 +263,27 @@ int tgemm_get_plan_info(tgemm_plan_t plan, tgemm_plan_info *info);
  * codes; sizes, dtypes, tiles and depths they reject are rejected here).  The
  * kernel's only memory besides A, B and C is its 16-byte status record; here it
  * lives in a fixed 256-byte array inside the library's CUDA module, which every
- * GPU that loads the library holds until the process exits.  A call that would
- * need more scratch than that array holds is rejected with
- * TGEMM_ERR_INVALID_ARG.  The call allocates nothing: no cudaMalloc, no
- * cudaFree, no allocating library routine.
+ * GPU that loads the library holds until the process exits.  The record always
+ * fits that array (the library checks this when it is compiled), so no size of
+ * problem needs more.  The call allocates nothing: no cudaMalloc, no cudaFree,
+ * no allocating library routine.
  *
  * The call enqueues on `stream` a clear of the array's status record and the
  * kernel.  If `status` is non-NULL it then copies the record back, waits for
- * `stream`, and stores TGEMM_OK or TGEMM_ERR_TIMEOUT there; if NULL the call
- * returns right after enqueueing.  All calls on a device share the one array:
- * calls whose kernels overlap on the same GPU (for instance on two streams)
- * race on it, and the status they report is then unreliable.
+ * `stream`, and stores TGEMM_OK or TGEMM_ERR_TIMEOUT there (or TGEMM_ERR_CHECK
+ * from a build with TGEMM_DEBUG_CHECKS=1); if NULL the call returns right after
+ * enqueueing.  Waiting for the stream is not allowed while it is being
+ * captured, so on a capturing stream a non-NULL `status` is rejected with
+ * TGEMM_ERR_INVALID_ARG before anything is enqueued.  All calls on a device
+ * share the one array: calls whose kernels overlap on the same GPU (for
+ * instance on two streams) race on it, and the status they report is then
+ * unreliable.
  *
- * The first call on each device looks up the array's device address and sets
- * the kernel's shared-memory ceiling for that device; make that first call
- * before any stream capture.
+ * Every call looks up the array's device address for the current device (a
+ * host-side lookup that allocates nothing), so a reset device or a new
+ * context is handled.  The first call on each device makes the runtime load
+ * the library's module there and sets the kernel's shared-memory ceiling for
+ * that device; make that first call before any stream capture.
  */
 int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N,
                       int block_K, int num_stages, const void *A, const void *B, void *C, tgemm_stream_t stream,

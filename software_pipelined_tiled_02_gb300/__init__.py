@@ -248,6 +248,7 @@ class Plan:
         self.pair = bool(pair)
         self.split_k = int(split_k)
         self.handle = h
+        self.lock = threading.Lock()  # a plan serves one host thread at a time
         self.M, self.N, self.K = M, N, K
         self.dtype, self.out_dtype = dtype, out_dtype
         self.block, self.num_stages = tuple(block), num_stages
@@ -369,15 +370,22 @@ def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=Non
     split_k = int(split_k or 1)
     group_m = int(group_m or 0)
     key = (M, N, K, dt, odt, tuple(block), num_stages, pair, split_k, group_m, A.device.index)
-    # A plan serves one host thread at a time (it caches tensor maps per pointer
-    # triple), so the lookup and the enqueue happen under the lock.
-    with _plans_lock:
-        plan = _plans.get(key)
-        if plan is None:
-            plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages, pair=pair, split_k=split_k,
-                                      group_m=group_m)
-            while len(_plans) > _PLANS_MAX:
-                _plans.popitem(last=False)[1].close()
-        else:
-            _plans.move_to_end(key)
-        return plan.run(A, B, out, stream)
+    # The cache lock covers the lookup only; the enqueue holds the plan's own
+    # lock (a plan caches tensor maps per pointer triple, so one host thread
+    # at a time), so threads running different plans do not serialise.
+    while True:
+        with _plans_lock:
+            plan = _plans.get(key)
+            if plan is None:
+                plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages, pair=pair, split_k=split_k,
+                                          group_m=group_m)
+                while len(_plans) > _PLANS_MAX:
+                    victim = _plans.popitem(last=False)[1]
+                    with victim.lock:  # waits for an enqueue in progress on it
+                        victim.close()
+            else:
+                _plans.move_to_end(key)
+        with plan.lock:
+            if plan.handle is None:  # evicted between the lookup and here: look up again
+                continue
+            return plan.run(A, B, out, stream)

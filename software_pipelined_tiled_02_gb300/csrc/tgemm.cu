@@ -470,7 +470,15 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                     wait_bar(full(j % S), uint32_t((j / S) & 1), p, abort, 0, j, false);
             } else {
                 // The odd CTA's loads complete the even CTA's barriers, which it
-                // cannot wait on: give them a fixed, generous time to land.
+                // cannot wait on (try_wait reads only this CTA's barriers), and
+                // the even CTA cannot wait on them either once it has aborted: a
+                // phase it never armed does not complete.  So the odd CTA gives
+                // its loads a fixed time to land.  At most S slots of at most
+                // 64 KB each are outstanding per CTA; even if every SM's ring
+                // were in flight at once (152 x 227 KB, about 35 MB) HBM at
+                // 6.7 TB/s delivers it in about 5 us, so 2 ms is a margin of
+                // several hundred.  This path runs only after a watchdog
+                // expiry, when the launch's result is already discarded.
                 const uint64_t t0 = globaltimer();
                 while (globaltimer() - t0 < 2000000ull) {
                 }
@@ -1228,26 +1236,25 @@ const char *tgemm_strerror(int code)
 
 static constexpr int kNoallocScratchInts = 64;  // 256 bytes; the kernel needs one 4-int record
 static __device__ __align__(256) int g_noalloc_scratch[kNoallocScratchInts];
+static constexpr size_t kNoallocRecordBytes = 4 * sizeof(int);  // code, role, block, iteration
+static_assert(kNoallocRecordBytes <= sizeof(g_noalloc_scratch), "the status record fits the fixed array");
 
-// Once per device, with that device current: the array's device address
-// (host code only sees a host-side stand-in for the symbol) and the kernel's
-// shared-memory ceiling.
+// Set-up with the calling device current: the array's device address and the
+// kernel's shared-memory ceiling.  Host code only sees a host-side stand-in for
+// the symbol, so the address comes from cudaGetSymbolAddress -- a host-side
+// lookup that allocates nothing.  It is looked up on every call rather than
+// cached per device ordinal: after cudaDeviceReset, or in another context on
+// the same device, the module is loaded again and the array may move.  The
+// first call on a device makes the runtime load the module there.
 static int noalloc_setup(int dev, int limit, int **scratch)
 {
-    static std::mutex mu;
-    static int *addr[64] = {};
-    if (dev < 0 || dev >= 64) return kErrInvalidArg;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return kErrCuda;
-        }
-        addr[dev] = static_cast<int *>(p);
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return kErrCuda;
     }
     if (allow_max_smem(dev, limit) != kOk) return kErrCuda;
-    *scratch = addr[dev];
+    *scratch = static_cast<int *>(p);
     return kOk;
 }
 
@@ -1255,8 +1262,6 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
                                  int block_K, int num_stages, const void *A, const void *B, void *C,
                                  tgemm_stream_t stream, int *status)
 {
-    const size_t need_bytes = 4 * sizeof(int);  // the status record
-    if (need_bytes > sizeof(g_noalloc_scratch)) return kErrInvalidArg;
     int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX);
     if (rc != kOk) return rc;
     int dev = 0, major = 0, minor = 0, sms = 0, limit = 0, per_sm = 0;
@@ -1271,7 +1276,18 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     if (major != 10 || minor != 3) return kErrArch;
     rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit);
     if (rc != kOk) return rc;
-    if (status) *status = kOk;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (status) {
+        // Reading the status back synchronises the stream, which a stream
+        // under capture does not allow: such a call must pass status = NULL.
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+            cudaGetLastError();
+            return kErrCuda;
+        }
+        if (cap != cudaStreamCaptureStatusNone) return kErrInvalidArg;
+        *status = kOk;
+    }
     if (M == 0 || N == 0) return kOk;  // empty product: nothing to write
     if (!C || (K > 0 && (!A || !B))) return kErrInvalidArg;
     if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return kErrAlignment;
@@ -1296,9 +1312,8 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     rc = encode_maps(q, L, dtype, out_dtype, A, B, C, nullptr);
     if (rc != kOk) return rc;
 
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // The array keeps the previous call's record: clear it before this launch.
-    if (cudaMemsetAsync(scratch, 0, need_bytes, s) != cudaSuccess) {
+    if (cudaMemsetAsync(scratch, 0, kNoallocRecordBytes, s) != cudaSuccess) {
         cudaGetLastError();
         return kErrCuda;
     }
@@ -1306,7 +1321,7 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     if (status) {
         int h[4] = {0, 0, 0, 0};
-        if (cudaMemcpyAsync(h, scratch, need_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        if (cudaMemcpyAsync(h, scratch, kNoallocRecordBytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
             cudaStreamSynchronize(s) != cudaSuccess) {
             cudaGetLastError();
             return kErrCuda;

@@ -18,14 +18,15 @@ def bits(C):
     return C.view(torch.int32 if C.element_size() == 4 else torch.int16)
 
 
-def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=False):
-    A, B = inputs.operands(seed, M, N, K, dtype, "normal")
+def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=False, group_m=0, split_k=1,
+                        dist="normal", kw=None):
+    A, B = inputs.operands(seed, M, N, K, dtype, dist, **(kw or {}))
     dA = inputs.bits_to_torch(A, dtype).cuda()
     dB = inputs.bits_to_torch(B, dtype).cuda()
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[out]
     res = []
     for s in stage_list:
-        plan = tg.Plan(M, N, K, dtype, out, block, s, pair=pair)
+        plan = tg.Plan(M, N, K, dtype, out, block, s, pair=pair, group_m=group_m, split_k=split_k)
         C = torch.full((M, N), float("nan"), dtype=tdt, device="cuda")
         plan.run(dA, dB, C)
         torch.cuda.synchronize()
@@ -45,6 +46,21 @@ def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=F
 @pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("bf16", "bf16")])
 def test_bit_identical_across_stages(cuda_lib, block, stage_list, dtype, out):
     res = outputs_over_stages(cuda_lib, 1000, 1040, 2056, dtype, out, block, stage_list, seed=77)
+    for s, C in zip(stage_list[1:], res[1:]):
+        assert torch.equal(bits(C), bits(res[0])), f"num_stages={s} differs"
+
+
+@pytest.mark.parametrize("name", ["gemm_4096_f16_normal", "gemm_8192_bf16_normal",
+                                  "gemm_4000x3000x5000_f16_uniform", "gemm_512x512x32768_f16_uniform"])
+def test_bit_identical_across_stages_benchmark_config(cuda_lib, name):
+    # The launch configuration the benchmark times (tile, CTA pair, raster
+    # group, K splits), at every depth that fits its tile.
+    w = inputs.WORKLOADS[name]
+    cfg = cuda_lib.default_config(w["M"], w["N"], w["K"], w["dtype"], w["out"])
+    stage_list = [s for s in (1, 2, 3, 4, 6) if s <= cfg["num_stages"]]
+    res = outputs_over_stages(cuda_lib, w["M"], w["N"], w["K"], w["dtype"], w["out"], cfg["block"], stage_list,
+                              w["seed"], pair=cfg["cta_pair"], group_m=cfg["group_m"], split_k=cfg["split_k"],
+                              dist=w["dist"], kw=w.get("kw"))
     for s, C in zip(stage_list[1:], res[1:]):
         assert torch.equal(bits(C), bits(res[0])), f"num_stages={s} differs"
 

@@ -83,3 +83,18 @@ def test_noalloc_rejects_what_the_plan_rejects(cuda_lib):
     assert tg.tgemm_run_noalloc(128, 128, 64, "f16", "f32", 64, 128, 32, 3, p, p, p)[0] == tg.ERR_NO_KERNEL
     assert tg.tgemm_run_noalloc(128, 128, 64, "f16", "f32", 128, 128, 32, 3, p + 2, p, p)[0] == tg.ERR_ALIGNMENT
     assert tg.tgemm_run_noalloc(0, 128, 64, "f16", "f32", 128, 128, 32, 3, 0, 0, 0) == (tg.OK, tg.OK)
+
+
+def test_noalloc_status_rejected_on_a_capturing_stream(cuda_lib):
+    # Reading the status back waits for the stream, which a capturing stream
+    # forbids: the call refuses before enqueueing anything.
+    tg = cuda_lib
+    x = torch.zeros(128 * 128, dtype=torch.float32, device="cuda")
+    p = x.data_ptr()
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=side):
+        rc, _ = tg.tgemm_run_noalloc(128, 128, 64, "f16", "f32", 128, 128, 32, 3, p, p, p, side.cuda_stream,
+                                     want_status=True)
+    assert rc == tg.ERR_INVALID_ARG
