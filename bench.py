@@ -54,6 +54,10 @@ def parse_args(argv=None):
     ap.add_argument("--pair", type=int, choices=(0, 1), default=None,
                     help="1: CTA pairs (clusters of 2) share each 256-row tile (default: tuned table)")
     ap.add_argument("--split-k", type=int, default=None, help="K splits per tile (default: tuned table)")
+    ap.add_argument("--cluster-k", type=int, default=None,
+                    help="K splits reduced inside the kernel by clusters of this many CTAs (default: tuned table)")
+    ap.add_argument("--stream-operands", type=int, choices=(0, 1), default=None,
+                    help="1: L2 evict-first hint on the operand loads (default: tuned table)")
     ap.add_argument("--group-m", type=int, default=None,
                     help="M-blocks per raster group of the persistent schedule (default: tuned table; 0 = 8)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -146,10 +150,12 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
-def config_key(block, stages, pair, split_k, group_m=8):
+def config_key(block, stages, pair, split_k, group_m=8, cluster_k=0, stream_operands=False):
     """The launch configuration as the ncu summaries record it."""
-    return (f"{block[0]},{block[1]},{block[2]} S{stages} pair{int(bool(pair))} split{int(split_k)} "
-            f"group{int(group_m) or 8}")
+    key = (f"{block[0]},{block[1]},{block[2]} S{stages} pair{int(bool(pair))} split{int(split_k)} "
+           f"group{int(group_m) or 8}")
+    key += f" cluster{int(cluster_k)}" if cluster_k and cluster_k > 1 else ""
+    return key + (" stream" if stream_operands else "")
 
 
 def recorded_traffic(workload, config=None):
@@ -359,6 +365,8 @@ def run_ours(args, w, world, rank, local):
         pair = bool(args.pair)
         split_k = args.split_k or 1
         group_m = args.group_m or 0
+        cluster_k = args.cluster_k or 0
+        stream_ops = bool(args.stream_operands)
     else:
         cfg = tg.default_config(M, N, K, w["dtype"], w["out"])
         block, stages, pair, split_k = cfg["block"], cfg["num_stages"], cfg["cta_pair"], cfg["split_k"]
@@ -369,13 +377,16 @@ def run_ours(args, w, world, rank, local):
             pair = bool(args.pair)
         if args.split_k is not None:
             split_k = args.split_k
+        cluster_k = cfg["cluster_k"] if args.cluster_k is None else args.cluster_k
+        stream_ops = cfg["stream_operands"] if args.stream_operands is None else bool(args.stream_operands)
     A, B = inputs.workload_operands(args.workload)
     hA = inputs.bits_to_torch(A, w["dtype"])
     hB = inputs.bits_to_torch(B, w["dtype"])
     dA, dB = hA.to(dev), hB.to(dev)
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[w["out"]]
     dC = torch.empty((M, N), dtype=tdt, device=dev)
-    plan = tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k, group_m=group_m)
+    plan = tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k, group_m=group_m,
+                   cluster_k=cluster_k, stream_operands=stream_ops)
     info = plan.info
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -435,7 +446,7 @@ def run_ours(args, w, world, rank, local):
         pA, pB = hA.pin_memory(), hB.pin_memory()
         pCs = [torch.empty((M, N), dtype=tdt).pin_memory() for _ in range(2)]
         plans = [plan, tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k,
-                               group_m=group_m)]
+                               group_m=group_m, cluster_k=cluster_k, stream_operands=stream_ops)]
         bufs = [(dA, dB, dC), (torch.empty_like(dA), torch.empty_like(dB), torch.empty_like(dC))]
         streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
         torch.cuda.synchronize(dev)
@@ -488,9 +499,10 @@ def run_ours(args, w, world, rank, local):
     algo_bytes = (M * K + N * K) * 2 + M * N * (4 if w["out"] == "f32" else 2)
     roofline = roofline_for(flops, algo_bytes, mean_ms / 1e3, measured_peaks())
     roofline.update({"traffic": recorded_traffic(args.workload,
-                                                 config_key(block, stages, pair, info["split_k"], group_m)),
+                                                 config_key(block, stages, pair, info["split_k"], group_m,
+                                                            info["cluster_k"], info["stream_operands"])),
                      "kernel": ("tgemm_kernel + splitk_reduce_kernel, timed together per step"
-                                if info["split_k"] > 1 else "tgemm_kernel"),
+                                if info["split_k"] > 1 and info["cluster_k"] <= 1 else "tgemm_kernel"),
                      "flops_per_launch": flops, "algorithmic_bytes_per_launch": algo_bytes})
 
     line = None
@@ -502,9 +514,12 @@ def run_ours(args, w, world, rank, local):
                 "warmup": args.warmup, "ms_per_step": max_mean_ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
                 "config": dict(config_block(args, w, block, stages), cta_pair=int(pair),
-                               split_k=int(info["split_k"]), group_m=int(group_m) or 8), "roofline": roofline,
+                               split_k=int(info["split_k"]), group_m=int(group_m) or 8,
+                               cluster_k=int(info["cluster_k"]),
+                               stream_operands=int(info["stream_operands"])), "roofline": roofline,
                 "cpu_baseline": cpu,
-                "e2e": e2e, "gpu_launches": args.steps * (2 if info["split_k"] > 1 else 1), "clocks": clocks,
+                "e2e": e2e, "gpu_launches": args.steps * (2 if info["split_k"] > 1 and info["cluster_k"] <= 1 else 1),
+                "clocks": clocks,
                 "sustained": sustained,
                 "plan": {k: info[k] for k in ("grid", "num_tiles", "smem_bytes", "tmem_columns", "acc_stages")},
                 "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms), "max": max(kernel_ms)}}

@@ -163,18 +163,45 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
  *     (chapter 11 sections 3.3 and 4.4): D = 1 serialises load and compute,
  *     D = 2 is the two-stage schedule of matmul_manual.  Results do not
  *     depend on D.
+ *   cluster_k: 0 or 1 = split K reduces through the workspace and a second
+ *     kernel, as above.  c = 2, 4 or 8 = the kernel reduces the splits itself:
+ *     one CTA per (tile, split) work unit, launched as thread-block clusters
+ *     of c CTAs that take c consecutive splits of one tile.  A cluster adds
+ *     its c partial accumulators through distributed shared memory, in rank
+ *     order; when split_k / c clusters share a tile, each writes its fp32 sum
+ *     to a workspace of (split_k / c) x ceil(M / 128) x 128 x N floats, and
+ *     the last to finish adds them in cluster order and writes C.  The order
+ *     of every sum depends only on the tile shape, split_k and c, so results
+ *     stay bit-identical across num_stages (they differ in rounding from the
+ *     two-kernel reduction, whose order is sequential).  Requires cta_pair = 0,
+ *     block_M = 128, an effective split count that is a multiple of c,
+ *     block_N / c a multiple of 32, and num_stages x (A + B slot) of at least
+ *     128 x block_N x 4 bytes (the exchanged partials land in the operand
+ *     ring); else INVALID_ARG (SMEM_BUDGET for the ring).  Launches of one such
+ *     plan must be ordered (one stream, or events between them): they share
+ *     the workspace and the arrival counters.
+ *   stream_operands: 0 = plain operand loads.  1 = the operand loads carry an
+ *     L2 evict-first hint: when L2 needs room, lines of A and B go before other
+ *     data (for instance dirty lines, whose eviction costs a write to HBM).
+ *     It pays when each operand line is read once, or by a few tiles at about
+ *     the same time (long K over few tiles); it costs where tiles of later
+ *     waves read the same rows again (large square problems).  Results do not
+ *     depend on it.  Other values: INVALID_ARG.
  */
 typedef struct tgemm_plan_opts {
     int cta_pair;
     int group_m;
     int split_k;
     int prefetch;
+    int cluster_k;
+    int stream_operands;
 } tgemm_plan_opts;
 
 /* tgemm_validate with options (NULL = defaults): the option ranges above
- * (cta_pair 0 or 1, group_m 0..4096, split_k 0..64, prefetch 0..num_stages)
- * give INVALID_ARG, then the checks of tgemm_validate and the split-K
- * workspace rule, as tgemm_plan_ex makes them. */
+ * (cta_pair 0 or 1, group_m 0..4096, split_k 0..64, prefetch 0..num_stages,
+ * cluster_k 0, 1, 2, 4 or 8, stream_operands 0 or 1) give INVALID_ARG, then the checks of
+ * tgemm_validate, the split-K workspace rule and the cluster_k rules, as
+ * tgemm_plan_ex makes them. */
 int tgemm_validate_ex(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M,
                       int block_N, int block_K, int num_stages, int64_t smem_limit,
                       const tgemm_plan_opts *opts);
@@ -214,6 +241,8 @@ int tgemm_run_host(tgemm_plan_t plan, const void *hA, const void *hB, void *hC, 
  * returns instead of hanging; C is undefined).  Negative ERR_CUDA on a failed
  * copy.  `detail` (may be NULL) receives 4 ints: code, warp role (0 producer,
  * 1 MMA, 2 epilogue), block index, and the pipeline iteration that timed out.
+ * For a plan with cluster_k > 1, a status other than TGEMM_OK also zeroes the
+ * plan's arrival counters, which a launch that gave up may have left part-way.
  */
 int tgemm_status(tgemm_plan_t plan, int *detail);
 
@@ -247,6 +276,8 @@ typedef struct tgemm_plan_info {
     int split_k;         /* effective K splits (1: none) */
     int num_units;       /* persistent work units: tiles x K splits */
     int prefetch;        /* producer lead in k-blocks */
+    int cluster_k;       /* > 1: K splits reduced in the kernel by clusters of this many CTAs */
+    int stream_operands; /* 1: operand loads carry an L2 evict-first hint */
 } tgemm_plan_info;
 
 int tgemm_get_plan_info(tgemm_plan_t plan, tgemm_plan_info *info);

@@ -130,8 +130,23 @@ inline int effective_splits(int64_t K, int bk, int splits)
     return int((kb + per - 1) / per);
 }
 
+// In-kernel split-K reduction (kernel mode 2): the K splits of a tile are
+// taken by clusters of csk CTAs, which exchange their partial accumulators
+// through distributed shared memory.  csk must be 2, 4 or 8 (clusters of up
+// to 8 are portable), with one CTA per 128-row tile, a whole number of
+// clusters per tile, and slices of block_N / csk columns that are whole
+// 32-column epilogue chunks.  Each CTA receives csk parts of 128 x slice
+// fp32 values, 128 x block_N x 4 bytes in all, into its operand ring.
+inline bool csplit_supported(int bm, int bn, int pair, int eff_splits, int csk)
+{
+    if (csk != 2 && csk != 4 && csk != 8) return false;
+    if (pair || bm != 128) return false;
+    if (eff_splits % csk != 0) return false;
+    return bn % csk == 0 && (bn / csk) % kEpiCols == 0;
+}
+
 inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int bm, int bn, int bk,
-                    int stages, int64_t smem_limit, int pair = 0, int splits = 1)
+                    int stages, int64_t smem_limit, int pair = 0, int splits = 1, int csk = 0)
 {
     if (dtype != kF16 && dtype != kBF16) return kErrUnsupportedDtype;
     if (out_dtype != kF32 && out_dtype != dtype) return kErrUnsupportedDtype;
@@ -152,10 +167,14 @@ inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, i
     // persistent schedule, with room for one more stride of CTAs.
     if (((M + bm - 1) / bm) * ((N + bn - 1) / bn) * int64_t(eff) > kMaxUnits) return kErrInvalidArg;
     if (stages > 64) return kErrSmemBudget;  // keeps the layout arithmetic in 32 bits
-    // A split-K kernel stages fp32 partial tiles whatever the final output type.
-    const int staged = eff > 1 ? kF32 : out_dtype;
+    if (csk > 1 && !csplit_supported(bm, bn, pair, eff, csk)) return kErrInvalidArg;
+    // A split-K kernel that reduces through the workspace stages fp32 partial
+    // tiles whatever the final output type.
+    const int staged = eff > 1 && csk <= 1 ? kF32 : out_dtype;
     Layout L = make_layout(bm, bn, bk, stages, dtype, staged, pair);
     if (L.bound > smem_limit || int64_t(L.total) > smem_limit) return kErrSmemBudget;
+    // The cluster exchange lands in the operand ring.
+    if (csk > 1 && int64_t(128) * bn * 4 > int64_t(L.off_c - L.off_a)) return kErrSmemBudget;
     return kOk;
 }
 

@@ -90,6 +90,14 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     unsigned long long watchdog_ns;
     int *status;                // 4 ints: code, role, block, iteration
     int debug_stall;
+    // In-kernel split-K reduction (kernel mode 2): the splits of a tile are
+    // taken by clusters of csk CTAs, outer = splits / csk clusters per tile.
+    int csk, outer;
+    int slice_w;                // output columns each CTA of a cluster reduces (block_N / csk)
+    float *ws;                  // outer > 1: [outer][split_rows][N] fp32 cluster partials
+    int *counters;              // outer > 1: [num_tiles][csk] arrival counts, zero between launches
+    void *C;                    // the output, written with plain stores in mode 2
+    int stream_ops;             // 1: operand loads carry an L2 evict-first hint
 };
 
 // ---------------------------------------------------------------- device side
@@ -258,12 +266,14 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
                 break;
             }
             tc_fence_after();
-            // slot s's operands lie inside the A and B rings; the accumulator inside TMEM
+            // slot s's operands lie inside the A and B rings; the accumulator inside TMEM.
+            // The descriptor holds address bits 4-17 of this CTA's shared window; in a
+            // cluster the window's addresses also carry the CTA's rank above them.
             const bool in_range =
-                check(uint32_t(ad & 0x3FFFu) << 4 >= c.sA && ((uint32_t(ad & 0x3FFFu) << 4) + p.a_slot) <=
-                                                                  c.sA + uint32_t(S) * p.a_slot &&
-                          uint32_t(bd & 0x3FFFu) << 4 >= c.sB &&
-                          ((uint32_t(bd & 0x3FFFu) << 4) + p.b_slot) <= c.sB + uint32_t(S) * p.b_slot &&
+                check(uint32_t(ad & 0x3FFFu) << 4 >= (c.sA & 0x3FFFFu) &&
+                          ((uint32_t(ad & 0x3FFFu) << 4) + p.a_slot) <= (c.sA & 0x3FFFFu) + uint32_t(S) * p.a_slot &&
+                          uint32_t(bd & 0x3FFFu) << 4 >= (c.sB & 0x3FFFFu) &&
+                          ((uint32_t(bd & 0x3FFFu) << 4) + p.b_slot) <= (c.sB & 0x3FFFFu) + uint32_t(S) * p.b_slot &&
                           (a + 1) * p.acc_cols <= p.tmem_cols && kb1 <= p.num_kb,
                       p, abort, 1, it);
             if (lane == 0 && in_range) {
@@ -321,16 +331,208 @@ __device__ __forceinline__ void mma_dispatch_nk(const Params &p, const MmaCtx &c
     }
 }
 
-// One kernel, two launch shapes.  PAIR = false: one CTA per tile.  PAIR =
-// true: clusters of two CTAs; the pair computes one block_M = 256 tile with
-// one M = 256 MMA per k-step issued by the even CTA, each CTA holding 128
-// rows of A, half of B's block_N rows and 128 rows of the accumulator.  The
-// pair shares one pipeline: both CTAs' TMA loads complete the even CTA's
-// full[s], and the even CTA's commits arrive on both CTAs' empty[s] and
-// acc_full[a]; both CTAs' epilogues arrive on the even CTA's acc_empty[a].
-template <bool PAIR>
+// Epilogue of kernel mode 2 (split K reduced inside the kernel).  This CTA
+// holds, in tensor memory, the fp32 partial sum of one K range of its tile
+// (128 rows x block_N columns); its cluster holds the csk consecutive K
+// ranges o*csk .. o*csk + csk-1 of the same tile, cluster rank r taking
+// range o*csk + r.
+//  1. Once its own MMAs are done, a cluster barrier: every CTA of the cluster
+//     has finished its K loop, so every operand ring in the cluster is idle.
+//  2. Reduce-scatter.  CTA r owns the tile's columns [r*slice_w, (r+1)*slice_w).
+//     Each CTA copies every 32-column chunk of its accumulator into the ring
+//     of the chunk's owner, into the region of its own rank
+//     (st.shared::cluster); a second cluster barrier makes the copies visible.
+//  3. The owner adds the csk parts of its slice in rank order 0, 1, ..., csk-1.
+//  4. outer = 1: it converts and stores the slice to C.  outer > 1: it stores
+//     the fp32 slice to the workspace region of its outer index o and counts
+//     in on the slice's counter; the CTA that counts last adds the outer
+//     partials in order o = 0, 1, ..., outer-1 (its own from shared memory,
+//     the others from the workspace), converts, stores to C and resets the
+//     counter.  No CTA waits for another outside its own cluster.
+// The order of every sum depends on the tile shape, csk and outer only: never
+// on num_stages, the schedule or which CTA arrives last.  Every path through
+// this function meets both cluster barriers, aborted or not.
+//
+// A part (one rank's 128 x slice_w values of a slice) is stored column group
+// by column group: the 16 bytes of row r, columns 4j .. 4j+3 sit at
+// (j * 128 + (r ^ (j % 8))) * 16.  A warp's copy of one column group (its 32
+// rows) is then 512 contiguous bytes of the owner's memory, and the owner's
+// threads, which take consecutive column groups of one row (so that their
+// global stores are contiguous), read eight different bank groups.
+
+// Items (16-byte column groups of one slice row) per epilogue thread:
+// 128 x slice_w / 4 over 256 threads = slice_w / 8, so 4, 8 or 16; a slice row
+// has 2 x NIT column groups.
+template <int NIT>
+__device__ __forceinline__ void csplit_finish(const Params &p, uint32_t sA, int *flag, int tile, int o,
+                                              uint32_t crank, int grow0, int gcol0, uint32_t part_bytes)
+{
+    constexpr int CPR = 2 * NIT;                 // column groups per slice row
+    const int et = int(threadIdx.x) - 2 * 32;  // 0..255 over the eight epilogue warps
+    // Item i of this thread: g = et + 256 i, slice row g / CPR, column group g % CPR.
+    auto row_of = [&](int i) { return (et + i * 8 * 32) / CPR; };
+    auto grp_of = [&](int i) { return (et + i * 8 * 32) % CPR; };
+    auto inside = [&](int i) { return grow0 + row_of(i) < p.M && gcol0 + 4 * grp_of(i) < p.N; };
+    auto elem = [&](int i) { return int64_t(grow0 + row_of(i)) * p.N + gcol0 + 4 * grp_of(i); };
+    // The cluster's sum of item i, parts added in rank order.
+    auto cluster_sum = [&](int i) -> float4 {
+        const int r = row_of(i), j = grp_of(i);
+        const uint32_t off = (uint32_t(j) * 128u + uint32_t(r ^ (j & 7))) << 4;
+        float4 acc = ld_shared_v4f(sA + off);
+        for (int src = 1; src < p.csk; ++src) {
+            const float4 t = ld_shared_v4f(sA + uint32_t(src) * part_bytes + off);
+            acc.x += t.x;
+            acc.y += t.y;
+            acc.z += t.z;
+            acc.w += t.w;
+        }
+        return acc;
+    };
+    const int64_t plane = int64_t(p.split_rows) * p.N;  // floats per outer region of the workspace
+    float4 tot[NIT];
+    if (p.outer > 1) {
+        float *wo = p.ws + int64_t(o) * plane;
+#pragma unroll
+        for (int i = 0; i < NIT; ++i)
+            if (inside(i)) *reinterpret_cast<float4 *>(wo + elem(i)) = cluster_sum(i);
+        __threadfence();  // this thread's partials are visible GPU-wide before the count below
+        named_bar_sync(1, 8 * 32);
+        if (et == 0) {
+            int *cnt = p.counters + tile * p.csk + int(crank);
+            const int last = atomicAdd(cnt, 1) == p.outer - 1;
+            if (last) *cnt = 0;  // every cluster of this launch has counted in: ready for the next launch
+            *flag = last;
+        }
+        named_bar_sync(1, 8 * 32);
+        if (!*reinterpret_cast<volatile int *>(flag)) return;
+        __threadfence();
+        // The total in the order o = 0, 1, ..., outer-1; for each outer index
+        // all of this thread's loads are issued before any is added.
+        for (int oo = 0; oo < p.outer; ++oo) {
+            float4 t[NIT];
+            if (oo == o) {
+#pragma unroll
+                for (int i = 0; i < NIT; ++i) t[i] = cluster_sum(i);
+            } else {
+                const float *wq = p.ws + int64_t(oo) * plane;
+#pragma unroll
+                for (int i = 0; i < NIT; ++i)  // items outside C read element 0 of the region, never stored
+                    t[i] = __ldcg(reinterpret_cast<const float4 *>(wq + (inside(i) ? elem(i) : 0)));
+            }
+#pragma unroll
+            for (int i = 0; i < NIT; ++i) {
+                if (oo == 0) {
+                    tot[i] = t[i];
+                } else {
+                    tot[i].x += t[i].x;
+                    tot[i].y += t[i].y;
+                    tot[i].z += t[i].z;
+                    tot[i].w += t[i].w;
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NIT; ++i) tot[i] = cluster_sum(i);
+    }
+#pragma unroll
+    for (int i = 0; i < NIT; ++i) {
+        if (!inside(i)) continue;
+        const int64_t e = elem(i);
+        const float4 acc = tot[i];
+        if (p.out_mode == 0) {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.C) + e) = acc;
+        } else if (p.out_mode == 1) {
+            __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(static_cast<__half *>(p.C) + e) = u;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.C) + e) = u;
+        }
+    }
+}
+
+__device__ __noinline__ void csplit_epilogue(const Params &p, uint32_t sA, int *flag, uint32_t tmem,
+                                             uint32_t acc_full0, volatile int *abort, int warp, int lane,
+                                             int unit)
+{
+    const int q = warp & 3;             // TMEM lane quarter: rows 32q .. 32q+31
+    const int sub = (warp - 2) >> 2;    // the two warps of a quarter take alternate chunks
+    const uint32_t crank = cluster_ctarank();
+    const int tile = unit / p.splits;
+    const int o = (unit - tile * p.splits) / p.csk;
+    const Unit w = unit_coords(p, unit);
+    const bool ok = unit < p.num_units && warp_wait(acc_full0, 0, p, abort, 2, 0);
+    tc_fence_after();
+    __syncwarp();
+    cluster_sync();  // 1: every ring of the cluster is idle
+    const uint32_t part_bytes = 128u * uint32_t(p.slice_w) * 4u;  // one rank's part of a slice
+    if (ok && !*abort) {
+        const int row = q * 32 + lane;
+        int idx = 0;
+        for (int c = 0; c * kEpiCols < p.bn; ++c) {
+            if ((idx++ & 1) != sub) continue;
+            const int owner = c * kEpiCols / p.slice_w;
+            const int j0 = (c * kEpiCols - owner * p.slice_w) / 4;  // first column group of the chunk in the slice
+            // the part lies inside the ring (the plan checks csk x part_bytes <= ring bytes)
+            if (!check(uint32_t(p.csk) * part_bytes <= p.off_c - p.off_a && owner < p.csk &&
+                           uint32_t(j0 + 8) * 128u * 16u <= part_bytes,
+                       p, abort, 2, c))
+                continue;
+            uint32_t v[32];
+            if (p.num_kb > 0) {
+                tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(c * kEpiCols), v);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0u;
+            }
+            const uint32_t dst = map_to_rank(sA + crank * part_bytes, uint32_t(owner));
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const uint32_t j = uint32_t(j0 + jj);
+                st_cluster_v4(dst + ((j * 128u + uint32_t(row ^ int(j & 7u))) << 4), v[4 * jj], v[4 * jj + 1],
+                              v[4 * jj + 2], v[4 * jj + 3]);
+            }
+        }
+    }
+    __syncwarp();
+    cluster_sync();  // 2: every part is in its owner's ring
+    if (!ok || *abort) return;
+    const int grow0 = w.mb * p.bm;
+    const int gcol0 = w.nb * p.bn + int(crank) * p.slice_w;
+    switch (p.slice_w) {
+    case 32: csplit_finish<4>(p, sA, flag, tile, o, crank, grow0, gcol0, part_bytes); break;
+    case 64: csplit_finish<8>(p, sA, flag, tile, o, crank, grow0, gcol0, part_bytes); break;
+    default: csplit_finish<16>(p, sA, flag, tile, o, crank, grow0, gcol0, part_bytes); break;
+    }
+}
+
+// One kernel, three launch shapes.
+//  MODE 0: one CTA per tile, persistent over work units.
+//  MODE 1: clusters of two CTAs; the pair computes one block_M = 256 tile
+//    with one M = 256 MMA per k-step issued by the even CTA, each CTA holding
+//    128 rows of A, half of B's block_N rows and 128 rows of the accumulator.
+//    The pair shares one pipeline: both CTAs' TMA loads complete the even
+//    CTA's full[s], and the even CTA's commits arrive on both CTAs' empty[s]
+//    and acc_full[a]; both CTAs' epilogues arrive on the even CTA's
+//    acc_empty[a].
+//  MODE 2: split K reduced inside the kernel.  One CTA per work unit (tile,
+//    K split), no persistence; the csk consecutive splits of a tile form one
+//    cluster, which sums its partial accumulators through distributed shared
+//    memory (csplit_epilogue); clusters of the same tile then combine through
+//    global memory, the last to arrive adding all in a fixed order.
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constant__ Params p)
 {
+    constexpr bool PAIR = MODE == 1;
+    constexpr bool CSPLIT = MODE == 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = (kSmemAlign - (raw & (kSmemAlign - 1))) & (kSmemAlign - 1);
@@ -397,6 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         // both complete the even CTA's full[s], which the even CTA arms with
         // the bytes of both.
         const uint32_t full_leader = PAIR ? map_to_rank(full(0), 0) : 0u;
+        // Streamed operands: each line is read by the tiles that share it at
+        // about the same time and not again, so it goes first when L2 needs room.
+        const uint64_t policy = p.stream_ops ? policy_evict_first() : 0ull;
         int s = 0;
         uint32_t ph = 0;
         int issued = 0;
@@ -437,19 +642,33 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                         if (rank == 0) mbar_arrive_expect_tx(full(s), p.stage_tx);
                         for (int pl = 0; pl < p.panels; ++pl) {
                             const int x = kb * p.bk + pl * p.panel_k;
-                            tma_load_2d_pair(a_dst + (uint32_t(pl) * p.a_panel16 << 4), &p.tmA, x, m0, fb);
-                            tma_load_2d_pair(b_dst + (uint32_t(pl) * p.b_panel16 << 4), &p.tmB, x, n0, fb);
+                            const uint32_t a_at = a_dst + (uint32_t(pl) * p.a_panel16 << 4);
+                            const uint32_t b_at = b_dst + (uint32_t(pl) * p.b_panel16 << 4);
                             // a wide tile's second N-half: this CTA's rows of it, block_N / 2 further on
-                            if (p.n_halves == 2)
-                                tma_load_2d_pair(b_dst + ((uint32_t(pl) * p.b_panel16 + p.b_half16) << 4), &p.tmB, x,
-                                                 n0 + (p.bn >> 1), fb);
+                            const uint32_t b2_at = b_dst + ((uint32_t(pl) * p.b_panel16 + p.b_half16) << 4);
+                            if (p.stream_ops) {
+                                tma_load_2d_pair_hint(a_at, &p.tmA, x, m0, fb, policy);
+                                tma_load_2d_pair_hint(b_at, &p.tmB, x, n0, fb, policy);
+                                if (p.n_halves == 2) tma_load_2d_pair_hint(b2_at, &p.tmB, x, n0 + (p.bn >> 1), fb, policy);
+                            } else {
+                                tma_load_2d_pair(a_at, &p.tmA, x, m0, fb);
+                                tma_load_2d_pair(b_at, &p.tmB, x, n0, fb);
+                                if (p.n_halves == 2) tma_load_2d_pair(b2_at, &p.tmB, x, n0 + (p.bn >> 1), fb);
+                            }
                         }
                     } else {
                         mbar_arrive_expect_tx(full(s), p.stage_tx);
                         for (int pl = 0; pl < p.panels; ++pl) {
                             const int x = kb * p.bk + pl * p.panel_k;
-                            tma_load_2d(a_dst + (uint32_t(pl) * p.a_panel16 << 4), &p.tmA, x, m0, full(s));
-                            tma_load_2d(b_dst + (uint32_t(pl) * p.b_panel16 << 4), &p.tmB, x, n0, full(s));
+                            const uint32_t a_at = a_dst + (uint32_t(pl) * p.a_panel16 << 4);
+                            const uint32_t b_at = b_dst + (uint32_t(pl) * p.b_panel16 << 4);
+                            if (p.stream_ops) {
+                                tma_load_2d_hint(a_at, &p.tmA, x, m0, full(s), policy);
+                                tma_load_2d_hint(b_at, &p.tmB, x, n0, full(s), policy);
+                            } else {
+                                tma_load_2d(a_at, &p.tmA, x, m0, full(s));
+                                tma_load_2d(b_at, &p.tmB, x, n0, full(s));
+                            }
                         }
                     }
                 }
@@ -485,6 +704,10 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
             }
         }
         __syncwarp();
+        if constexpr (CSPLIT) {  // the two cluster barriers of csplit_epilogue
+            cluster_sync();
+            cluster_sync();
+        }
     } else if (warp == 1) {
         // ---------------- MMA issuer: the warp runs the loop, lane 0 drives the tensor core.
         // The k-steps per slot and the MMAs per k-step are compile-time in
@@ -496,6 +719,13 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
             else
                 mma_dispatch_nk<1, PAIR>(p, c, abort, lane);
         }
+        if constexpr (CSPLIT) {  // the two cluster barriers of csplit_epilogue
+            __syncwarp();
+            cluster_sync();
+            cluster_sync();
+        }
+    } else if constexpr (CSPLIT) {
+        csplit_epilogue(p, sA, reinterpret_cast<int *>(smem + p.off_c), tmem, acc_full(0), abort, warp, lane, unit0);
     } else {
         // ---------------- epilogue: 8 warps; warp w reads TMEM lanes 32*(w%4)..+31,
         // and the two warps of a lane quarter take alternate 32-column chunks.
@@ -724,7 +954,9 @@ struct tgemm_plan_s {
     int tiles_m, tiles_n, num_tiles, grid, group_m;
     int pair;  // clusters of two CTAs per block_M = 256 tile
     int splits;                // K splits (1: none)
-    float *d_work;             // split-K partial sums, splits x M x N fp32 (owned by the plan)
+    int csk;                   // > 1: splits reduced inside the kernel by clusters of csk CTAs
+    float *d_work;             // split-K partial sums: splits (or, with csk, splits / csk) x M x N fp32
+    int *d_counters;           // csk with more than one cluster per tile: arrival counters
     int *d_status;
     unsigned long long watchdog_ns;
     int debug_stall;
@@ -746,9 +978,9 @@ static int allow_max_smem(int dev, int limit)
     static bool done[64] = {};
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && done[dev]) return kOk;
-    if (cudaFuncSetAttribute(tgemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(tgemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess) {
+    if (cudaFuncSetAttribute(tgemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess ||
+        cudaFuncSetAttribute(tgemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess ||
+        cudaFuncSetAttribute(tgemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess) {
         cudaGetLastError();
         return kErrCuda;
     }
@@ -761,7 +993,7 @@ static int allow_max_smem(int dev, int limit)
 // splits; prefetch: the producer's lead in k-blocks.
 static void fill_params(Params &q, const Layout &L, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
                         int block_M, int block_N, int block_K, int num_stages, int pair, int splits, int prefetch,
-                        int group_m, int tiles_m, int tiles_n)
+                        int group_m, int tiles_m, int tiles_n, int csk = 0)
 {
     std::memset(&q, 0, sizeof(q));
     q.M = int(M);
@@ -795,8 +1027,12 @@ static void fill_params(Params &q, const Layout &L, int64_t M, int64_t N, int64_
     q.acc_step = L.n_halves == 2 ? uint32_t(block_N / 2) : uint32_t(block_N);
     q.a_half16 = L.m_halves == 2 ? (128u * uint32_t(L.swizzle_bytes)) >> 4 : 0u;
     q.b_half16 = L.n_halves == 2 ? (uint32_t(q.b_box_rows) * uint32_t(L.swizzle_bytes)) >> 4 : 0u;
-    // The kernel's own output: fp32 partials when K is split, else C's type.
-    q.out_mode = splits > 1 ? 0 : out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
+    // The kernel's own output: fp32 partials when K is split and reduced by a
+    // second kernel, else C's type.
+    q.out_mode = splits > 1 && csk <= 1 ? 0 : out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
+    q.csk = csk > 1 ? csk : 0;
+    q.outer = csk > 1 ? splits / csk : 1;
+    q.slice_w = csk > 1 ? block_N / csk : 0;
     q.acc_stages = L.acc_stages;
     q.acc_cols = L.acc_cols;
     q.tmem_cols = L.tmem_cols;
@@ -848,7 +1084,7 @@ static int encode_maps(Params &q, const Layout &L, int dtype, int out_dtype, con
                            operand_promotion(pitch));
     }
     if (rc != kOk) return rc;
-    if (q.splits > 1)
+    if (q.splits > 1 && q.csk == 0)
         return encode_2d(&q.tmC, kF32, work, N, uint64_t(q.splits) * uint64_t(q.split_rows), N * 4u,
                          uint32_t(kEpiCols), 32u, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     return encode_2d(&q.tmC, out_dtype, C, N, M, N * uint64_t(L.out_bytes), uint32_t(kEpiCols), 32u,
@@ -864,6 +1100,10 @@ static int check_opts(const tgemm_plan_opts *opts, int num_stages)
     if (opts->group_m < 0 || opts->group_m > 4096) return kErrInvalidArg;
     if (opts->split_k < 0 || opts->split_k > kMaxSplits) return kErrInvalidArg;
     if (opts->prefetch < 0 || opts->prefetch > num_stages) return kErrInvalidArg;
+    if (opts->cluster_k != 0 && opts->cluster_k != 1 && opts->cluster_k != 2 && opts->cluster_k != 4 &&
+        opts->cluster_k != 8)
+        return kErrInvalidArg;
+    if (opts->stream_operands != 0 && opts->stream_operands != 1) return kErrInvalidArg;
     return kOk;
 }
 
@@ -922,7 +1162,8 @@ int tgemm_validate_ex(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
     const int rc = check_opts(opts, num_stages);
     if (rc != kOk) return rc;
     return validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit,
-                    opts ? opts->cta_pair : 0, opts && opts->split_k > 1 ? opts->split_k : 1);
+                    opts ? opts->cta_pair : 0, opts && opts->split_k > 1 ? opts->split_k : 1,
+                    opts && opts->cluster_k > 1 ? opts->cluster_k : 0);
 }
 
 int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N,
@@ -939,8 +1180,9 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     const int pair = opts && opts->cta_pair ? 1 : 0;
     if (check_opts(opts, num_stages) != kOk) return kErrInvalidArg;
     const int splits = effective_splits(K, block_K, opts && opts->split_k > 1 ? opts->split_k : 1);
+    const int csk = opts && opts->cluster_k > 1 ? opts->cluster_k : 0;
     // Argument checks that need no device come first.
-    int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX, pair, splits);
+    int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX, pair, splits, csk);
     if (rc != kOk) return rc;
     int dev = 0, major = 0, minor = 0, sms = 0, limit = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
@@ -952,7 +1194,7 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
         return kErrCuda;
     }
     if (major != 10 || minor != 3) return kErrArch;
-    rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit, pair, splits);
+    rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit, pair, splits, csk);
     if (rc != kOk) return rc;
 
     tgemm_plan_s *p = new (std::nothrow) tgemm_plan_s();
@@ -962,11 +1204,14 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     p->K = K;
     p->dtype = dtype;
     p->out_dtype = out_dtype;
-    // With K splits the kernel stages fp32 partial tiles; the reduction converts.
-    p->L = make_layout(block_M, block_N, block_K, num_stages, dtype, splits > 1 ? kF32 : out_dtype, pair);
+    // With K splits reduced by a second kernel, the kernel stages fp32 partial
+    // tiles and the reduction converts.
+    p->L = make_layout(block_M, block_N, block_K, num_stages, dtype, splits > 1 && !csk ? kF32 : out_dtype, pair);
     p->pair = pair;
     p->splits = splits;
+    p->csk = csk;
     p->d_work = nullptr;
+    p->d_counters = nullptr;
     p->device = dev;
     p->num_sms = sms;
     p->smem_limit = limit;
@@ -1011,7 +1256,7 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, tgemm_kernel<true>, &cfg) != cudaSuccess || clusters < 1) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, tgemm_kernel<1>, &cfg) != cudaSuccess || clusters < 1) {
             cudaGetLastError();
             cudaFree(p->d_status);
             delete p;
@@ -1019,10 +1264,46 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
         }
         p->grid = 2 * (units < clusters ? units : clusters);
     }
-    if (splits > 1) {
-        const size_t bytes = size_t(splits) * size_t(p->tiles_m) * size_t(block_M) * size_t(N) * sizeof(float);
+    if (csk) {
+        // One CTA per work unit (not persistent): clusters of csk never wait on
+        // one another, so the grid may take several waves.  At least one
+        // cluster must fit.
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = unsigned(csk);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(unsigned(units), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = size_t(p->smem_launch);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, tgemm_kernel<2>, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            cudaFree(p->d_status);
+            delete p;
+            return kErrCuda;
+        }
+        p->grid = units;
+    }
+    const int outer = csk ? splits / csk : splits;  // partial sums that go through the workspace
+    if (splits > 1 && outer > 1) {
+        const size_t bytes = size_t(outer) * size_t(p->tiles_m) * size_t(block_M) * size_t(N) * sizeof(float);
         if (cudaMalloc(&p->d_work, bytes) != cudaSuccess) {
             cudaGetLastError();
+            cudaFree(p->d_status);
+            delete p;
+            return kErrCuda;
+        }
+    }
+    if (csk && outer > 1) {
+        const size_t bytes = size_t(p->num_tiles) * size_t(csk) * sizeof(int);
+        if (cudaMalloc(&p->d_counters, bytes) != cudaSuccess || cudaMemset(p->d_counters, 0, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            if (p->d_counters) cudaFree(p->d_counters);
+            if (p->d_work) cudaFree(p->d_work);
             cudaFree(p->d_status);
             delete p;
             return kErrCuda;
@@ -1031,9 +1312,12 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
 
     Params &q = p->params;
     fill_params(q, p->L, M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, pair, splits,
-                opts && opts->prefetch > 0 ? opts->prefetch : num_stages, p->group_m, p->tiles_m, p->tiles_n);
+                opts && opts->prefetch > 0 ? opts->prefetch : num_stages, p->group_m, p->tiles_m, p->tiles_n, csk);
     q.watchdog_ns = p->watchdog_ns;
     q.status = p->d_status;
+    q.ws = p->d_work;
+    q.counters = p->d_counters;
+    q.stream_ops = opts && opts->stream_operands ? 1 : 0;
     *out = p;
     return kOk;
 }
@@ -1051,6 +1335,7 @@ static int prepare_maps(tgemm_plan_s *p, const void *A, const void *B, void *C)
     p->cA = A;
     p->cB = B;
     p->cC = C;
+    p->params.C = C;
     p->maps_valid = true;
     return kOk;
 }
@@ -1065,11 +1350,11 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
     if (rc != kOk) return rc;
     p->params.watchdog_ns = p->watchdog_ns;
     p->params.debug_stall = p->debug_stall;
-    if (p->pair) {
+    if (p->pair || p->csk) {
         cudaLaunchConfig_t cfg{};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = p->csk ? unsigned(p->csk) : 2u;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(unsigned(p->grid), 1, 1);
@@ -1078,15 +1363,15 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
         cfg.stream = reinterpret_cast<cudaStream_t>(stream);
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, tgemm_kernel<true>, p->params) != cudaSuccess) {
+        if (cudaLaunchKernelEx(&cfg, p->csk ? tgemm_kernel<2> : tgemm_kernel<1>, p->params) != cudaSuccess) {
             cudaGetLastError();
             return kErrCuda;
         }
     } else {
-        tgemm_kernel<false><<<p->grid, kThreads, p->smem_launch, reinterpret_cast<cudaStream_t>(stream)>>>(p->params);
+        tgemm_kernel<0><<<p->grid, kThreads, p->smem_launch, reinterpret_cast<cudaStream_t>(stream)>>>(p->params);
         if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     }
-    if (p->splits > 1) {
+    if (p->splits > 1 && !p->csk) {
         const int64_t mn = p->M * p->N;
         const int64_t n4 = mn / 4;
         int blocks = int((n4 + 255) / 256);
@@ -1136,6 +1421,13 @@ int tgemm_status(tgemm_plan_t p, int *detail)
         cudaGetLastError();
         return -kErrCuda;
     }
+    // A launch that gave up may have left some of the in-kernel split
+    // reduction's arrival counters part-way: clear them for the next launch.
+    if (h[0] != kOk && p->d_counters &&
+        cudaMemset(p->d_counters, 0, size_t(p->num_tiles) * size_t(p->csk) * sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return -kErrCuda;
+    }
     if (detail) std::memcpy(detail, h, sizeof(h));
     return h[0];
 }
@@ -1182,6 +1474,8 @@ int tgemm_get_plan_info(tgemm_plan_t p, tgemm_plan_info *info)
     info->split_k = p->splits;
     info->prefetch = p->params.prefetch;
     info->num_units = p->params.num_units;
+    info->cluster_k = p->csk;
+    info->stream_operands = p->params.stream_ops;
     return kOk;
 }
 
@@ -1194,6 +1488,10 @@ int tgemm_destroy(tgemm_plan_t p)
         rc = kErrCuda;
     }
     if (p->d_work && cudaFree(p->d_work) != cudaSuccess) {
+        cudaGetLastError();
+        rc = kErrCuda;
+    }
+    if (p->d_counters && cudaFree(p->d_counters) != cudaSuccess) {
         cudaGetLastError();
         rc = kErrCuda;
     }
@@ -1317,7 +1615,7 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
         cudaGetLastError();
         return kErrCuda;
     }
-    tgemm_kernel<false><<<grid, kThreads, smem, s>>>(q);
+    tgemm_kernel<0><<<grid, kThreads, smem, s>>>(q);
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     if (status) {
         int h[4] = {0, 0, 0, 0};

@@ -12,17 +12,28 @@ pages say of cost models; the sweep decides.
 
 from __future__ import annotations
 
-# (M, N, K, operand dtype, out dtype) -> (block, num_stages[, cta_pair[, split_k[, group_m]]]);
-# dtype codes 0 f16, 1 bf16, 2 f32; group_m is the persistent raster's group of
-# M-blocks (0: the library's 8).  The figures are same-GPU, interleaved
-# timings against the runner-up.
+# (M, N, K, operand dtype, out dtype) -> launch configuration; dtype codes 0
+# f16, 1 bf16, 2 f32.  Keys left out take their defaults (DEFAULT_OPTS):
+# cta_pair, split_k (K splits), group_m (the persistent raster's group of
+# M-blocks; 0: the library's 8), cluster_k (> 1: K splits reduced inside the
+# kernel by clusters of that many CTAs) and stream_operands (L2 evict-first
+# hint on the operand loads).  The comments give same-GPU, interleaved timings
+# against the runner-up.
 FROZEN = {
-    (4096, 4096, 4096, 0, 0): ((256, 224, 128), 3, True, 1, 2),  # 1643 vs 1607 for one CTA 256x224x64, group 8
-    (8192, 8192, 8192, 1, 1): ((256, 256, 128), 3, True),       # 1753 vs 1692 for one CTA 256x256x64
-    (4000, 3000, 5000, 0, 2): ((256, 384, 64), 4, True),        # 94.0 vs 100.1 us for 256x224x64 S6 (96.9 vs 99.0 at S5)
-    (512, 512, 32768, 0, 2): ((256, 256, 128), 3, True, 19),    # 514 vs 485 for 128x128x64 S6 split 9; 107 unsplit
-    (128, 128, 128, 0, 2): ((128, 128, 32), 3),
+    # 1643 vs 1607 TFLOP/s for one CTA 256x224x64, group 8
+    (4096, 4096, 4096, 0, 0): dict(block=(256, 224, 128), num_stages=3, cta_pair=True, group_m=2),
+    # 1753 vs 1692 for one CTA 256x256x64
+    (8192, 8192, 8192, 1, 1): dict(block=(256, 256, 128), num_stages=3, cta_pair=True),
+    # 94.2 vs 96.3 us without the evict-first hint; 96.3 vs 100.1 for 256x224x64 S6
+    (4000, 3000, 5000, 0, 2): dict(block=(256, 384, 64), num_stages=4, cta_pair=True, stream_operands=True),
+    # 31.2 vs 33.3 us without the evict-first hint; 35.4 for 128x128x64 S6 split 9; 166 unsplit;
+    # the in-kernel cluster reduction (128x256x64 S4, split 16, clusters of 4) 38.9
+    (512, 512, 32768, 0, 2): dict(block=(256, 256, 128), num_stages=3, cta_pair=True, split_k=19,
+                                  stream_operands=True),
+    (128, 128, 128, 0, 2): dict(block=(128, 128, 32), num_stages=3),
 }
+
+DEFAULT_OPTS = dict(cta_pair=False, split_k=1, group_m=0, cluster_k=0, stream_operands=False)
 
 # Candidate tiles: (block, depth, relative steady-state throughput per SM
 # measured at full waves on GB300 with one CTA 256x256 = 1, CTA pair).  A
@@ -57,10 +68,9 @@ def estimate(M: int, N: int, K: int, block, rel: float, num_sms: int = DEFAULT_S
 
 
 def choose(M: int, N: int, K: int, dtype: int, out_dtype: int, num_sms: int = DEFAULT_SMS) -> dict:
-    """{block, num_stages, cta_pair, split_k, group_m} for a problem."""
+    """{block, num_stages, cta_pair, split_k, group_m, cluster_k, stream_operands} for a problem."""
     hit = FROZEN.get((M, N, K, dtype, out_dtype))
     if hit is not None:
-        return {"block": hit[0], "num_stages": hit[1], "cta_pair": hit[2] if len(hit) > 2 else False,
-                "split_k": hit[3] if len(hit) > 3 else 1, "group_m": hit[4] if len(hit) > 4 else 0}
+        return dict(DEFAULT_OPTS, **hit)
     best = min(CANDIDATES, key=lambda c: (estimate(M, N, K, c[0], c[2], num_sms, c[3]), -c[2]))
-    return {"block": best[0], "num_stages": best[1], "cta_pair": best[3], "split_k": 1, "group_m": 0}
+    return dict(DEFAULT_OPTS, block=best[0], num_stages=best[1], cta_pair=best[3])

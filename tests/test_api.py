@@ -48,7 +48,7 @@ C_PROGRAM = r"""
 
 int main(void)
 {
-    tgemm_plan_opts opts = {1, 2, 1, 0};  /* cta_pair, group_m, split_k, prefetch */
+    tgemm_plan_opts opts = {1, 2, 1, 0, 0, 0};  /* cta_pair, group_m, split_k, prefetch, cluster_k, stream */
     int64_t bound = tgemm_smem_bound(TGEMM_F16, 128, 128, 32, 3);
     int one = tgemm_validate(4096, 4096, 4096, TGEMM_F16, TGEMM_F16, 256, 224, 64, 3, 232448);
     int pair = tgemm_validate_ex(4096, 4096, 4096, TGEMM_F16, TGEMM_F16, 256, 224, 128, 3, 232448, &opts);
@@ -190,6 +190,38 @@ def test_validate_ex_options(lib):
     assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, L, prefetch=4) == tg.OK
     # a split count above the number of k-blocks is cut down first, so it is not an error
     assert V(M, 4, 2 * 32, tg.F16, tg.F32, 128, 32, 32, 4, L, split_k=64) == tg.OK
+
+
+def test_validate_ex_stream_operands(lib):
+    V = tg.tgemm_validate_ex
+    for v, want in ((0, tg.OK), (1, tg.OK), (2, tg.ERR_INVALID_ARG), (-1, tg.ERR_INVALID_ARG)):
+        assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, LIMIT_227K, stream_operands=v) == want
+
+
+def test_validate_ex_cluster_k_rules(lib):
+    # Splits reduced inside the kernel by clusters of cluster_k CTAs.
+    V = tg.tgemm_validate_ex
+    L = LIMIT_227K
+    ok = dict(split_k=16, cluster_k=4)
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 4, L, **ok) == tg.OK
+    assert V(512, 512, 32768, tg.F16, tg.F16, 128, 256, 64, 4, L, **ok) == tg.OK
+    for c in (0, 1, 2, 4, 8):
+        assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 4, L, split_k=16, cluster_k=c) == tg.OK
+    for c in (3, 5, 16, -1):  # only 2, 4 and 8 (portable cluster sizes) or off
+        assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 4, L, split_k=16, cluster_k=c) == tg.ERR_INVALID_ARG
+    # one CTA per 128-row tile only
+    assert V(512, 512, 32768, tg.F16, tg.F32, 256, 256, 128, 3, L, cta_pair=1, **ok) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 32768, tg.F16, tg.F32, 256, 128, 64, 3, L, **ok) == tg.ERR_INVALID_ARG
+    # a whole number of clusters per tile, after the split count is cut to the k-blocks
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 4, L, split_k=18, cluster_k=4) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 64 * 6, tg.F16, tg.F32, 128, 256, 64, 4, L, split_k=8, cluster_k=4) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 64 * 8, tg.F16, tg.F32, 128, 256, 64, 4, L, split_k=8, cluster_k=4) == tg.OK
+    # slices of block_N / cluster_k columns must be whole 32-column chunks
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 128, 64, 4, L, split_k=16, cluster_k=8) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 96, 64, 4, L, split_k=16, cluster_k=2) == tg.ERR_INVALID_ARG
+    # the exchanged partials (128 x block_N x 4 bytes) must fit the operand ring
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 2, L, **ok) == tg.ERR_SMEM_BUDGET  # 96 KB < 128 KB
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 3, L, **ok) == tg.OK              # 144 KB
 
 
 def test_budget_rule_agrees_with_oracle_over_the_grid(lib):

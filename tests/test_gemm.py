@@ -24,10 +24,11 @@ def to_dev(bits, dtype):
     return inputs.bits_to_torch(bits, dtype).cuda()
 
 
-def run(tg, A, B, dtype, out, block, stages, pair=False, split_k=1, group_m=0):
+def run(tg, A, B, dtype, out, block, stages, pair=False, split_k=1, group_m=0, cluster_k=0):
     M, K = A.shape
     N = B.shape[0]
-    plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair, split_k=split_k, group_m=group_m)
+    plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair, split_k=split_k, group_m=group_m,
+                   cluster_k=cluster_k)
     dA, dB = to_dev(A, dtype), to_dev(B, dtype)
     C = torch.full((M, N), float("nan"), dtype=TORCH[out], device="cuda")
     plan.run(dA, dB, C)
@@ -304,12 +305,12 @@ def full_size(cuda_lib, name, block=None, stages=None, pair=False, split_k=1):
     """The workload in the launch configuration the benchmark times (the tuned default)."""
     w = inputs.WORKLOADS[name]
     A, B = inputs.workload_operands(name)
-    group_m = 0
+    group_m = cluster_k = 0
     if block is None:
         cfg = cuda_lib.default_config(w["M"], w["N"], w["K"], w["dtype"], w["out"])
         block, stages, pair, split_k = cfg["block"], cfg["num_stages"], cfg["cta_pair"], cfg["split_k"]
-        group_m = cfg["group_m"]
-    C = run(cuda_lib, A, B, w["dtype"], w["out"], block, stages, pair, split_k, group_m)
+        group_m, cluster_k = cfg["group_m"], cfg["cluster_k"]
+    C = run(cuda_lib, A, B, w["dtype"], w["out"], block, stages, pair, split_k, group_m, cluster_k)
     return w, A, B, C
 
 
@@ -386,3 +387,96 @@ def test_run_host_argument_errors(cuda_lib):
     torch.cuda.synchronize()
     assert plan.status()[0] == 0 and not hC.any()
     plan.close()
+
+
+# ------------------------------------------------------------ split K reduced inside the kernel
+
+# (block, num_stages, split_k, cluster_k): clusters of 2, 4 and 8 CTAs, one to
+# three clusters per tile (outer = split_k / cluster_k), slices of 128, 64 and
+# 32 columns.
+CSPLIT_CONFIGS = [
+    ((128, 256, 64), 4, 16, 4),
+    ((128, 256, 64), 3, 8, 8),
+    ((128, 256, 128), 2, 4, 4),
+    ((128, 256, 64), 4, 6, 2),
+    ((128, 128, 64), 4, 8, 4),
+    ((128, 64, 32), 5, 2, 2),
+    ((128, 256, 32), 6, 24, 8),
+]
+
+
+def csplit_k(block, split_k, per_split):
+    # per_split k-blocks per split, the last k-block ragged (8 columns short,
+    # zero-filled by the loads), so that the split count stays split_k
+    return per_split * split_k * block[2] - 8
+
+
+@pytest.mark.parametrize("block,stages,split_k,cluster_k", CSPLIT_CONFIGS, ids=lambda v: str(v))
+@pytest.mark.parametrize("shape", [(300, 520, 2), (129, 264, 3), (512, 512, 4), (1, 64, 1)],
+                         ids=lambda s: "%dx%dxk%d" % s)
+@pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("bf16", "bf16"), ("f16", "f16")])
+def test_cluster_split_parity(cuda_lib, block, stages, split_k, cluster_k, shape, dtype, out):
+    M, N, per = shape
+    K = csplit_k(block, split_k, per)
+    assert cuda_lib.tgemm_validate_ex(M, N, K, dtype, out, *block, stages, 232448, split_k=split_k,
+                                      cluster_k=cluster_k) == cuda_lib.OK
+    A, B = inputs.operands(300 + M + N + K, M, N, K, dtype, "uniform")
+    C = as_f64(run(cuda_lib, A, B, dtype, out, block, stages, split_k=split_k, cluster_k=cluster_k))
+    R, S = oracle.gemm(A, B, dtype)
+    assert_close(C, R, S, out)
+
+
+@pytest.mark.parametrize("block,stages,split_k,cluster_k", CSPLIT_CONFIGS, ids=lambda v: str(v))
+def test_cluster_split_integer_exact_repeatable_and_stage_invariant(cuda_lib, block, stages, split_k, cluster_k):
+    # Integer inputs: every order of summation gives the exact result.  The
+    # same plan launched again (its counters reset by the last cluster of each
+    # tile) and plans of other depths give the same bits.
+    M, N, K = 300, 520, csplit_k(block, split_k, 3)
+    A, B = inputs.operands(41, M, N, K, "f16", "int", lo=-4, hi=4)
+    dA, dB = to_dev(A, "f16"), to_dev(B, "f16")
+    R, _ = oracle.gemm(A, B, "f16")
+    outs = []
+    for s in sorted({1, 2, stages}):
+        try:
+            plan = cuda_lib.Plan(M, N, K, "f16", "f32", block, s, split_k=split_k, cluster_k=cluster_k)
+        except cuda_lib.TgemmError as e:  # a ring too small for the exchange at this depth
+            assert e.code == cuda_lib.ERR_SMEM_BUDGET and s < stages
+            continue
+        assert plan.info["cluster_k"] == cluster_k
+        for _ in range(2):
+            outs.append(plan.run(dA, dB))
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+        plan.close()
+    assert outs
+    assert np.array_equal(as_f64(outs[0]), R)
+    for C in outs[1:]:
+        assert torch.equal(C, outs[0])
+    # random values: bit-identical across depths and launches as well
+    A, B = inputs.operands(42, M, N, K, "bf16", "normal")
+    dA, dB = to_dev(A, "bf16"), to_dev(B, "bf16")
+    outs = []
+    for s in sorted({1, 2, stages}):
+        if cuda_lib.tgemm_validate_ex(M, N, K, "bf16", "bf16", *block, s, 232448, split_k=split_k,
+                                      cluster_k=cluster_k) != cuda_lib.OK:
+            continue
+        plan = cuda_lib.Plan(M, N, K, "bf16", "bf16", block, s, split_k=split_k, cluster_k=cluster_k)
+        outs += [plan.run(dA, dB), plan.run(dA, dB)]
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+        plan.close()
+    for C in outs[1:]:
+        assert torch.equal(C.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_cluster_split_long_k_full_and_integer(cuda_lib):
+    # The long-reduction workload in cluster mode, whatever the tuned default is.
+    for name in ("gemm_512x512x32768_f16_uniform", "gemm_512x512x32768_f16_int"):
+        w = inputs.WORKLOADS[name]
+        A, B = inputs.workload_operands(name)
+        C = as_f64(run(cuda_lib, A, B, w["dtype"], w["out"], (128, 256, 64), 4, split_k=16, cluster_k=4))
+        R, S = oracle.gemm(A, B, w["dtype"])
+        if w["dist"] == "int":
+            assert np.array_equal(C, R)
+        else:
+            assert_close(C, R, S, w["out"])

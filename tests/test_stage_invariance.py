@@ -19,14 +19,15 @@ def bits(C):
 
 
 def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=False, group_m=0, split_k=1,
-                        dist="normal", kw=None):
+                        dist="normal", kw=None, cluster_k=0):
     A, B = inputs.operands(seed, M, N, K, dtype, dist, **(kw or {}))
     dA = inputs.bits_to_torch(A, dtype).cuda()
     dB = inputs.bits_to_torch(B, dtype).cuda()
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[out]
     res = []
     for s in stage_list:
-        plan = tg.Plan(M, N, K, dtype, out, block, s, pair=pair, group_m=group_m, split_k=split_k)
+        plan = tg.Plan(M, N, K, dtype, out, block, s, pair=pair, group_m=group_m, split_k=split_k,
+                       cluster_k=cluster_k)
         C = torch.full((M, N), float("nan"), dtype=tdt, device="cuda")
         plan.run(dA, dB, C)
         torch.cuda.synchronize()
@@ -57,10 +58,14 @@ def test_bit_identical_across_stages_benchmark_config(cuda_lib, name):
     # group, K splits), at every depth that fits its tile.
     w = inputs.WORKLOADS[name]
     cfg = cuda_lib.default_config(w["M"], w["N"], w["K"], w["dtype"], w["out"])
-    stage_list = [s for s in (1, 2, 3, 4, 6) if s <= cfg["num_stages"]]
+    stage_list = [s for s in (1, 2, 3, 4, 6) if s <= cfg["num_stages"] and
+                  cuda_lib.tgemm_validate_ex(w["M"], w["N"], w["K"], w["dtype"], w["out"], *cfg["block"], s, 232448,
+                                             cta_pair=int(cfg["cta_pair"]), split_k=cfg["split_k"],
+                                             cluster_k=cfg["cluster_k"]) == cuda_lib.OK]
+    assert len(stage_list) >= 2
     res = outputs_over_stages(cuda_lib, w["M"], w["N"], w["K"], w["dtype"], w["out"], cfg["block"], stage_list,
                               w["seed"], pair=cfg["cta_pair"], group_m=cfg["group_m"], split_k=cfg["split_k"],
-                              dist=w["dist"], kw=w.get("kw"))
+                              dist=w["dist"], kw=w.get("kw"), cluster_k=cfg["cluster_k"])
     for s, C in zip(stage_list[1:], res[1:]):
         assert torch.equal(bits(C), bits(res[0])), f"num_stages={s} differs"
 
@@ -137,3 +142,22 @@ def test_bit_identical_across_raster_groups(cuda_lib):
             plan.close()
         for C in res[1:]:
             assert torch.equal(bits(C), bits(res[0]))
+
+
+@pytest.mark.parametrize("block,stages,pair,split_k", [((128, 256, 64), 4, False, 1), ((256, 224, 128), 3, True, 1),
+                                                       ((256, 384, 64), 4, True, 1), ((256, 256, 128), 3, True, 5)])
+def test_stream_operands_changes_nothing_but_the_cache_policy(cuda_lib, block, stages, pair, split_k):
+    # The evict-first hint on the operand loads only steers L2 replacement.
+    M, N, K = 1000, 1040, 2056
+    A, B = inputs.operands(83, M, N, K, "f16", "normal")
+    dA = inputs.bits_to_torch(A, "f16").cuda()
+    dB = inputs.bits_to_torch(B, "f16").cuda()
+    res = []
+    for stream in (False, True):
+        plan = cuda_lib.Plan(M, N, K, "f16", "f32", block, stages, pair=pair, split_k=split_k, stream_operands=stream)
+        assert plan.info["stream_operands"] == int(stream)
+        res.append(plan.run(dA, dB))
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+        plan.close()
+    assert torch.equal(bits(res[0]), bits(res[1]))

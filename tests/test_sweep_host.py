@@ -79,9 +79,11 @@ def test_frozen_defaults_are_legal_and_chosen():
 
     for (M, N, K, dt, od), entry in defaults.FROZEN.items():
         cfg = defaults.choose(M, N, K, dt, od)
-        assert cfg["block"] == entry[0] and cfg["num_stages"] == entry[1]
+        assert all(cfg[k] == v for k, v in entry.items())
+        assert set(cfg) == {"block", "num_stages"} | set(defaults.DEFAULT_OPTS)
         rc = tg.tgemm_validate_ex(M, N, K, dt, od, *cfg["block"], cfg["num_stages"], 232448,
-                                  cta_pair=int(cfg["cta_pair"]), split_k=cfg["split_k"], group_m=cfg["group_m"])
+                                  cta_pair=int(cfg["cta_pair"]), split_k=cfg["split_k"], group_m=cfg["group_m"],
+                                  cluster_k=cfg["cluster_k"], stream_operands=int(cfg["stream_operands"]))
         assert rc == tg.OK, ((M, N, K), cfg, tg.strerror(rc))
 
 

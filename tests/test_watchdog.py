@@ -16,15 +16,17 @@ from software_pipelined_tiled_02_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("block,stages,pair", [((128, 128, 32), 3, False), ((128, 256, 64), 1, False),
-                                               ((256, 256, 64), 4, True)])
-def test_stall_reports_timeout_and_context_survives(cuda_lib, block, stages, pair):
+@pytest.mark.parametrize("block,stages,pair,split_k,cluster_k", [
+    ((128, 128, 32), 3, False, 1, 0), ((128, 256, 64), 1, False, 1, 0), ((256, 256, 64), 4, True, 1, 0),
+    ((128, 256, 64), 4, False, 8, 4),  # K splits reduced in the kernel by clusters of 4: both cluster levels
+])
+def test_stall_reports_timeout_and_context_survives(cuda_lib, block, stages, pair, split_k, cluster_k):
     M, N, K = 512, 512, 512
     A, B = inputs.operands(31, M, N, K, "f16", "uniform")
     dA = inputs.bits_to_torch(A, "f16").cuda()
     dB = inputs.bits_to_torch(B, "f16").cuda()
     C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
-    plan = cuda_lib.Plan(M, N, K, "f16", "f32", block, stages, pair=pair)
+    plan = cuda_lib.Plan(M, N, K, "f16", "f32", block, stages, pair=pair, split_k=split_k, cluster_k=cluster_k)
     plan.set_watchdog_ns(50_000_000)
     plan.debug_stall(True)
     plan.run(dA, dB, C)
