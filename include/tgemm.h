@@ -101,8 +101,10 @@ int tgemm_smem_limit(void);
  *     coordinate); num_stages >= 1; at most 2^30 output
  *     tiles (times K splits)                               -> INVALID_ARG
  *   - K % 8 == 0, N * out_bytes % 16 == 0 (row pitch)      -> ALIGNMENT
- *   - block_M in {128, 256}; block_N a multiple of 32 in
- *     [32, 256] (with cta_pair also 320, 384, 448, 512);
+ *   - block_M in {64, 128, 256} (64: M = 64 tensor-core
+ *     instructions; cta_pair: 256 only); block_N a multiple
+ *     of 32 in [32, 256] (with cta_pair also 320, 384, 448,
+ *     512);
  *     block_K in {16, 32, 64, 128} (16-bit
  *     operands: rows of 32, 64 or 128 bytes, or two 128-byte
  *     K-panels for 128)                                     -> NO_KERNEL

@@ -44,7 +44,8 @@ struct Layout {
     uint32_t bar_bytes;
     uint32_t total;          // bytes requested, including alignment slack
     int64_t bound;           // stages * (A tile + B tile): the budget rule's bound
-    int m_halves;            // bm / 128 MMAs of M = 128 per k-step
+    int m_halves;            // MMAs along M per k-step: 2 for a one-CTA 256-row tile, else 1
+    int quarter_rows;        // accumulator rows per TMEM lane quarter: 32, or 16 for 64-row tiles
     int n_halves;            // pair tiles wider than one MMA (block_N > 256): two MMAs of N = block_N / 2
     int acc_cols;            // TMEM columns of one accumulator (m_halves * bn)
     int acc_stages;          // accumulators in flight (2 lets the epilogue overlap the next tile)
@@ -55,8 +56,9 @@ struct Layout {
 
 inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Tile shapes the kernel implements: M = 128 MMAs (one or two per k-step),
-// N a multiple of 32 up to the MMA maximum of 256, and block_K such that a
+// Tile shapes the kernel implements: M = 64 or M = 128 MMAs (a 256-row tile
+// issues two M = 128 MMAs per k-step), N a multiple of 32 up to the MMA
+// maximum of 256, and block_K such that a
 // K-contiguous operand row is one swizzle span (32, 64 or 128 bytes) or two
 // 128-byte spans (block_K = 128 for 16-bit operands: the slot then holds two
 // K-panels of 64 elements, each a standard 128-byte-swizzled tile).  The
@@ -67,7 +69,7 @@ inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 inline bool tile_supported(int bm, int bn, int bk, int in_bytes, int pair = 0)
 {
     if (pair && bm != 256) return false;
-    if (bm != 128 && bm != 256) return false;
+    if (bm != 64 && bm != 128 && bm != 256) return false;
     const bool wide = pair && bn > 256 && bn <= 512 && bn % 64 == 0;
     if (!wide && (bn < 32 || bn > 256 || bn % 32 != 0)) return false;
     int row = bk * in_bytes;
@@ -102,7 +104,10 @@ inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out
     L.off_bar = L.off_c + round_up(uint32_t(kEpiWarps * L.epi_bufs) * L.c_buf_bytes, kSmemAlign);
     L.bar_bytes = barrier_block_bytes(stages);
     L.total = L.off_bar + L.bar_bytes + kSmemAlign;  // slack to align the dynamic base
-    L.m_halves = pair ? 1 : bm / 128;
+    L.m_halves = pair || bm < 256 ? 1 : 2;
+    // An M = 64 accumulator keeps its rows in lanes 0-15 of each 32-lane
+    // quarter of tensor memory: row r in lane 32 * (r / 16) + r % 16.
+    L.quarter_rows = bm == 64 ? 16 : 32;
     L.n_halves = pair && bn > 256 ? 2 : 1;
     L.acc_cols = L.m_halves * bn;
     L.acc_stages = (2 * L.acc_cols <= kTmemColsMax) ? 2 : 1;

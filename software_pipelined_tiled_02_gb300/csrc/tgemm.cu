@@ -67,7 +67,10 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     int num_units;              // work units: num_tiles * splits
     int bm, bn, bk, stages;
     int n_kstep;                // bk / 16 MMAs along K per slot
-    int m_halves;               // bm / 128 (1 in pair mode: one M = 256 MMA covers both CTAs)
+    int m_halves;               // MMAs along M per k-step: 2 for a one-CTA 256-row tile, else 1
+                                // (pair mode: one M = 256 MMA covers both CTAs)
+    int quarter_rows;           // accumulator rows per TMEM lane quarter: 32, or 16 for M = 64
+                                // (lanes 0-15 of each quarter hold them)
     int mma_per_kstep;          // MMAs per k-step: 2 M-halves (one CTA, bm = 256), 2 N-halves
                                 // (pair, bn > 256), else 1
     uint32_t acc_step;          // TMEM columns between the accumulators of the two MMAs
@@ -745,7 +748,9 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
             tc_fence_after();
             int idx = 0;
             for (int h = 0; h < p.m_halves; ++h) {
-                const int row0 = m0 + h * 128 + q * 32;
+                // this warp's accumulator rows: quarter_rows of them, from TMEM lane 32q;
+                // with 16 rows (M = 64) lanes 16-31 load and stage values the store leaves out
+                const int row0 = m0 + h * 128 + q * p.quarter_rows;
                 if (row0 >= p.M) continue;  // warp-uniform
                 for (int c = 0; c * kEpiCols < p.bn; ++c) {
                     const int col0 = n0 + c * kEpiCols;
@@ -1016,6 +1021,7 @@ static void fill_params(Params &q, const Layout &L, int64_t M, int64_t N, int64_
     q.stages = num_stages;
     q.n_kstep = block_K * L.in_bytes / 32;  // one MMA consumes K = 16 elements = 32 bytes
     q.m_halves = L.m_halves;
+    q.quarter_rows = L.quarter_rows;
     q.a_rows = L.a_rows;
     q.b_rows = L.b_rows;
     q.n_halves = L.n_halves;
@@ -1041,7 +1047,7 @@ static void fill_params(Params &q, const Layout &L, int64_t M, int64_t N, int64_
     // 0), N >> 3 (bits 17-22), M >> 4 (bits 24-28): M = 128 for one CTA,
     // M = 256 for the CTA pair.
     const uint32_t ab = dtype == kBF16 ? 1u : 0u;
-    const uint32_t mma_m = pair ? 256u : 128u;
+    const uint32_t mma_m = pair ? 256u : block_M == 64 ? 64u : 128u;
     const uint32_t mma_n = uint32_t(block_N / L.n_halves);
     q.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((mma_n >> 3) << 17) | ((mma_m >> 4) << 24);
     q.a_slot = round_up(L.a_stage_bytes, kSmemAlign);
@@ -1084,10 +1090,12 @@ static int encode_maps(Params &q, const Layout &L, int dtype, int out_dtype, con
                            operand_promotion(pitch));
     }
     if (rc != kOk) return rc;
+    // one store box per epilogue chunk: kEpiCols columns of one warp's accumulator rows
+    const uint32_t box_rows = uint32_t(L.quarter_rows);
     if (q.splits > 1 && q.csk == 0)
         return encode_2d(&q.tmC, kF32, work, N, uint64_t(q.splits) * uint64_t(q.split_rows), N * 4u,
-                         uint32_t(kEpiCols), 32u, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
-    return encode_2d(&q.tmC, out_dtype, C, N, M, N * uint64_t(L.out_bytes), uint32_t(kEpiCols), 32u,
+                         uint32_t(kEpiCols), box_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    return encode_2d(&q.tmC, out_dtype, C, N, M, N * uint64_t(L.out_bytes), uint32_t(kEpiCols), box_rows,
                      L.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
@@ -1508,7 +1516,7 @@ const char *tgemm_strerror(int code)
     case kErrAlignment: return "pointer or row pitch not a multiple of 16 bytes";
     case kErrSmemBudget: return "num_stages x (A tile + B tile) exceeds the per-block shared-memory limit";
     case kErrNoKernel:
-        return "tile shape not implemented (block_M 128/256, block_N 32..256 step 32, block_K 16/32/64/128; "
+        return "tile shape not implemented (block_M 64/128/256, block_N 32..256 step 32, block_K 16/32/64/128; "
                "CTA pairs need block_M 256)";
     case kErrArch: return "device is not compute capability 10.3 (GB300)";
     case kErrCuda: return "CUDA runtime or driver call failed";

@@ -14,11 +14,19 @@ autotuning", restated for this kernel:
   1e-2 (the fp64 oracle is test infrastructure, kept out of this tool);
 * section 3.8: read the config, not the latency: the winner (lowest median
   time; ties within 1 % go to the smaller shared footprint, then to fewer
-  stages) is written to a per-device cache file, and a switch
-  (TGEMM_AUTOTUNE_DISABLE_CACHE=1) forces a new search;
+  stages) is written to a per-device cache directory as best_config.json,
+  beside latency.json with every candidate's timing, footprint and check.
+  A later search of the same workload on the same device reads the cached
+  winner instead of timing anything; the switch
+  TGEMM_AUTOTUNE_DISABLE_CACHE=1 (or --no-cache) forces a new search;
 * the num_stages experiment of the "01-num-stages-ir-diff" README: latency
   and shared memory against num_stages for several tile shapes, where
   latency should plateau while shared memory keeps growing.
+
+The prune is reported twice: with the pages' own budget, 228 KiB for
+num_stages x (A tile + B tile) (section 4.5; 214 of 216 configs at 4096^3,
+section 3.7), and with this device's queried limit and this kernel's rules
+(its real footprint, the tile shapes it implements).
 
 Usage (on a GB300):
     python -m software_pipelined_tiled_02_gb300.sweep --workload gemm_4096_f16_normal --space gb300
@@ -47,9 +55,24 @@ GB300_SPACE = dict(block_M=(128, 256), block_N=(64, 128, 192, 224, 256, 384, 512
                    num_stages=(2, 3, 4, 5, 6, 8), cta_pair=(0, 1))
 
 
+PAGES_BUDGET = 228 * 1024  # the pages' per-block shared-memory budget (H100)
+
+
+def pages_prune_count(configs, M, N, K, dtype, budget=PAGES_BUDGET, divisible=True):
+    """How many configs the pages' own rule keeps: the tile divides the
+    problem and num_stages x (A tile + B tile) fits the budget."""
+    kept = 0
+    for c in configs:
+        if divisible and (M % c["block_M"] or N % c["block_N"] or K % c["block_K"]):
+            continue
+        if tg.tgemm_smem_bound(dtype, c["block_M"], c["block_N"], c["block_K"], c["num_stages"]) <= budget:
+            kept += 1
+    return kept
+
+
 def enumerate_space(space: dict):
-    keys = ("block_M", "block_N", "block_K", "num_stages", "cta_pair")
-    vals = [space.get(k, (0,)) for k in keys]
+    keys = ("block_M", "block_N", "block_K", "num_stages", "cta_pair", "split_k", "stream_operands")
+    vals = [space.get(k, (1,) if k == "split_k" else (0,)) for k in keys]
     out = [dict(zip(keys, v)) for v in itertools.product(*vals)]
     # CTA pairs exist only for block_M = 256 tiles.
     return [c for c in out if not (c["cta_pair"] and c["block_M"] != 256)]
@@ -65,7 +88,9 @@ def prune(configs, M, N, K, dtype, out_dtype, smem_limit, divisible=True):
             rejects["not_divisible"].append(c)
             continue
         rc = tg.tgemm_validate_ex(M, N, K, dtype, out_dtype, c["block_M"], c["block_N"], c["block_K"],
-                                  c["num_stages"], smem_limit, cta_pair=c.get("cta_pair", 0))
+                                  c["num_stages"], smem_limit, cta_pair=c.get("cta_pair", 0),
+                                  split_k=c.get("split_k", 1), cluster_k=c.get("cluster_k", 0),
+                                  stream_operands=c.get("stream_operands", 0))
         if rc == tg.OK:
             legal.append(c)
         elif rc == tg.ERR_SMEM_BUDGET:
@@ -87,20 +112,44 @@ def pick_best(rows):
     return min(near, key=lambda r: (r["smem_bytes"], r["num_stages"], r["median_ms"]))
 
 
-def cache_path(device_name: str, workload: str) -> str:
+def cache_dir(device_name: str, workload: str) -> str:
+    """Per-device, per-workload cache directory (TGEMM_CACHE_DIR, default ~/.cache/tgemm)."""
     base = os.environ.get("TGEMM_CACHE_DIR", os.path.join(os.path.expanduser("~"), ".cache", "tgemm"))
     safe = "".join(ch if ch.isalnum() else "_" for ch in device_name)
-    return os.path.join(base, safe, f"{workload}.best_config.json")
+    return os.path.join(base, safe, workload)
+
+
+def cache_path(device_name: str, workload: str, name: str = "best_config.json") -> str:
+    return os.path.join(cache_dir(device_name, workload), name)
+
+
+def cache_disabled() -> bool:
+    return os.environ.get("TGEMM_AUTOTUNE_DISABLE_CACHE") == "1"
 
 
 def load_cached(device_name: str, workload: str):
-    if os.environ.get("TGEMM_AUTOTUNE_DISABLE_CACHE") == "1":
+    if cache_disabled():
         return None
     try:
         with open(cache_path(device_name, workload)) as f:
             return json.load(f)
     except (OSError, ValueError):
         return None
+
+
+def write_cache(device_name: str, workload: str, best: dict, rows: list):
+    """best_config.json (the winner) and latency.json (every candidate)."""
+    os.makedirs(cache_dir(device_name, workload), exist_ok=True)
+    keys = ("block_M", "block_N", "block_K", "num_stages", "cta_pair", "split_k", "cluster_k", "stream_operands",
+            "prefetch", "median_ms", "min_ms", "tflops", "smem_bytes", "smem_bound", "ok", "worst_error_ratio",
+            "error")
+    lat = [{k: r[k] for k in keys if k in r} for r in rows]
+    for name, obj in (("best_config.json", best), ("latency.json", lat)):
+        path = cache_path(device_name, workload, name)
+        tmp = path + f".{os.getpid()}.tmp"
+        with open(tmp, "w") as f:
+            json.dump(obj, f, indent=1)
+        os.replace(tmp, path)
 
 
 class Runner:
@@ -137,7 +186,8 @@ class Runner:
         try:
             plan = tg.Plan(self.M, self.N, self.K, w["dtype"], w["out"],
                            (c["block_M"], c["block_N"], c["block_K"]), c["num_stages"], pair=bool(c.get("cta_pair")),
-                           prefetch=int(c.get("prefetch", 0)))
+                           prefetch=int(c.get("prefetch", 0)), split_k=int(c.get("split_k", 1) or 1),
+                           cluster_k=int(c.get("cluster_k", 0)), stream_operands=bool(c.get("stream_operands")))
         except tg.TgemmError as e:
             row.update(ok=False, error=str(e))
             return row
@@ -190,9 +240,15 @@ def main(argv=None):
     ap.add_argument("--stage-curve", action="store_true", help="latency and smem vs num_stages for 3 tile shapes")
     ap.add_argument("--prefetch-curve", action="store_true",
                     help="latency vs the producer's prefetch distance at a fixed number of buffers")
+    ap.add_argument("--tiles", default=None, help="only these tiles, e.g. 128x128x32,256x224x128")
+    ap.add_argument("--stages", default=None, help="only these num_stages, e.g. 2,3,4")
+    ap.add_argument("--split-k", default=None, help="K splits to try, e.g. 1,9,19 (default 1)")
+    ap.add_argument("--stream", action="store_true", help="also try the L2 evict-first operand hint")
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--out", default=None, help="write all rows as JSON here")
-    ap.add_argument("--no-cache", action="store_true", help="do not write the per-device best config")
+    ap.add_argument("--no-cache", action="store_true",
+                    help="neither read nor write the per-device cache (same as TGEMM_AUTOTUNE_DISABLE_CACHE=1 "
+                         "for reading)")
     args = ap.parse_args(argv)
 
     import torch
@@ -202,8 +258,18 @@ def main(argv=None):
     M, N, K = w["M"], w["N"], w["K"]
     limit = tg.tgemm_smem_limit()
     dev = torch.cuda.get_device_name()
-    runner = Runner(args.workload, reps=args.reps)
     report = {"workload": args.workload, "device": dev, "smem_limit": limit}
+    if not (args.stage_curve or args.prefetch_curve or args.no_cache):
+        cached = load_cached(dev, args.workload)
+        if cached is not None:
+            report.update(cache_hit=True, best=cached, cache=cache_dir(dev, args.workload))
+            print("cache hit:", json.dumps(cached), flush=True)
+            if args.out:
+                with open(args.out, "w") as f:
+                    json.dump(report, f, indent=1)
+            return report
+    report["cache_hit"] = False
+    runner = Runner(args.workload, reps=args.reps)
 
     if args.prefetch_curve:
         curve = []
@@ -252,14 +318,28 @@ def main(argv=None):
                       f"model's sufficient depth = {f['min_depth']}")
         report["model_fit"] = fits
     else:
-        space = PAGES_SPACE if args.space == "pages" else GB300_SPACE
+        space = dict(PAGES_SPACE if args.space == "pages" else GB300_SPACE)
+        if args.tiles:
+            tiles = [tuple(int(v) for v in t.split("x")) for t in args.tiles.split(",")]
+            space.update(block_M=sorted({t[0] for t in tiles}), block_N=sorted({t[1] for t in tiles}),
+                         block_K=sorted({t[2] for t in tiles}))
+        if args.stages:
+            space["num_stages"] = tuple(int(v) for v in args.stages.split(","))
+        if args.split_k:
+            space["split_k"] = tuple(int(v) for v in args.split_k.split(","))
+        if args.stream:
+            space["stream_operands"] = (0, 1)
         configs = enumerate_space(space)
+        if args.tiles:
+            configs = [c for c in configs if (c["block_M"], c["block_N"], c["block_K"]) in tiles]
         legal, rejects = prune(configs, M, N, K, w["dtype"], w["out"], limit, divisible=not args.any_tile)
         report["requested"] = len(configs)
+        report["pages_prune"] = {"budget": PAGES_BUDGET, "kept": pages_prune_count(
+            configs, M, N, K, w["dtype"], divisible=not args.any_tile)}
         report["legal"] = len(legal)
         report["rejected"] = {k: len(v) for k, v in rejects.items()}
-        print(json.dumps({k: report[k] for k in ("workload", "device", "smem_limit", "requested", "legal",
-                                                 "rejected")}), flush=True)
+        print(json.dumps({k: report[k] for k in ("workload", "device", "smem_limit", "requested", "pages_prune",
+                                                 "legal", "rejected")}), flush=True)
         rows = [runner.run(c) for c in legal]
         report["rows"] = rows
         best = pick_best(rows)
@@ -268,10 +348,8 @@ def main(argv=None):
             print(json.dumps({k: r.get(k) for k in ("block_M", "block_N", "block_K", "num_stages", "cta_pair",
                                                     "median_ms", "tflops", "smem_bytes", "ok")}), flush=True)
         if best and not args.no_cache:
-            path = cache_path(dev, args.workload)
-            os.makedirs(os.path.dirname(path), exist_ok=True)
-            with open(path, "w") as f:
-                json.dump(best, f, indent=1)
+            write_cache(dev, args.workload, best, rows)
+            report["cache"] = cache_dir(dev, args.workload)
         print("best:", json.dumps(best), flush=True)
         bad = [r for r in rows if not r.get("ok")]
         if bad:
@@ -279,6 +357,7 @@ def main(argv=None):
     if args.out:
         with open(args.out, "w") as f:
             json.dump(report, f, indent=1)
+    return report
 
 
 if __name__ == "__main__":

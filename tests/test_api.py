@@ -156,7 +156,9 @@ def test_validate_rules(lib):
     assert V(128, 132, 128, tg.F16, tg.F32, 128, 128, 32, 3, L) == tg.OK      # 528-byte fp32 rows
     assert V(128, 132, 128, tg.F16, tg.F16, 128, 128, 32, 3, L) == tg.ERR_ALIGNMENT  # 264-byte fp16 rows
     # tile shapes the kernel implements
-    assert V(128, 128, 128, tg.F16, tg.F32, 64, 128, 32, 3, L) == tg.ERR_NO_KERNEL
+    assert V(128, 128, 128, tg.F16, tg.F32, 64, 128, 32, 3, L) == tg.OK  # M = 64 instructions
+    assert V(128, 128, 128, tg.F16, tg.F32, 96, 128, 32, 3, L) == tg.ERR_NO_KERNEL
+    assert V(128, 128, 128, tg.F16, tg.F32, 32, 128, 32, 3, L) == tg.ERR_NO_KERNEL
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 48, 32, 3, L) == tg.ERR_NO_KERNEL
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 512, 32, 3, L) == tg.ERR_NO_KERNEL
     assert V(128, 128, 128, tg.F16, tg.F32, 128, 128, 128, 1, L) == tg.OK  # two 64-wide K-panels per slot
@@ -246,7 +248,7 @@ def test_plan_without_device_fails_cleanly(lib):
     # argument errors are reported before any device query
     rc, h = tg.tgemm_plan(128, 128, 128, tg.F16, tg.F32, 128, 128, 32, 0)
     assert rc == tg.ERR_INVALID_ARG and h is None
-    rc, h = tg.tgemm_plan(128, 128, 128, tg.F16, tg.F32, 64, 128, 32, 2)
+    rc, h = tg.tgemm_plan(128, 128, 128, tg.F16, tg.F32, 96, 128, 32, 2)
     assert rc == tg.ERR_NO_KERNEL and h is None
     assert tg.tgemm_smem_limit() < 0
     assert tg.tgemm_destroy(None) == tg.OK

@@ -59,6 +59,10 @@ def test_gemm_128_f16_uniform_tile_128x128x32_s3(cuda_lib):
 
 
 CONFIGS = [
+    ((64, 128, 32), 3),     # M = 64 instructions: 16 accumulator rows per TMEM lane quarter
+    ((64, 256, 64), 4),
+    ((64, 64, 16), 2),
+    ((64, 96, 128), 3),
     ((128, 128, 32), 3),
     ((128, 256, 64), 4),
     ((256, 128, 64), 3),

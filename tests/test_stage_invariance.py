@@ -43,6 +43,7 @@ def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=F
     ((256, 128, 64), (1, 2, 3)),
     ((128, 64, 16), (1, 2, 4, 8)),
     ((128, 128, 128), (1, 2, 3)),
+    ((64, 128, 64), (1, 2, 4, 6)),
 ])
 @pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("bf16", "bf16")])
 def test_bit_identical_across_stages(cuda_lib, block, stage_list, dtype, out):

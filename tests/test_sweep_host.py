@@ -22,11 +22,10 @@ def test_pages_space_prunes_over_budget_before_launch():
     assert (256, 256, 64, 4) in over
     # every config the pages' bound puts over the limit is rejected, none is launched
     for c in cfgs:
-        if c["block_M"] != 64 and oracle.smem_bound(c["block_M"], c["block_N"], c["block_K"],
-                                                    c["num_stages"], 2) > LIMIT:
+        if oracle.smem_bound(c["block_M"], c["block_N"], c["block_K"], c["num_stages"], 2) > LIMIT:
             assert c not in legal
-    # block_M = 64 is not implemented by this kernel: reported, not launched
-    assert all(c["block_M"] == 64 for c in rej["no_kernel"]) and rej["no_kernel"]
+    # the kernel implements every tile shape of the pages' grid (block_M 64 included)
+    assert not rej["no_kernel"]
     assert not rej["not_divisible"]
     assert len(legal) + sum(len(v) for v in rej.values()) == len(cfgs)
 
@@ -95,3 +94,29 @@ def test_wide_pair_tiles_only_in_pair_mode():
     no_kernel = {key(c) for c in rej["no_kernel"]}
     assert (256, 512, 64, 4, 1) in ok and (256, 512, 64, 5, 1) not in ok   # 48 KB slots: four fit
     assert (256, 512, 64, 2, 0) in no_kernel and (128, 384, 64, 2, 0) in no_kernel
+
+
+def test_pages_prune_count_matches_the_pages():
+    # Chapter 11 section 3.7: 216 configs at 4096^3 (the grid below times the
+    # two `threads` values), of which 214 are kept; the two rejects are
+    # 256x256x64 at 4 stages (256 KiB > 228 KiB).
+    cfgs = sweep.enumerate_space(sweep.PAGES_SPACE)
+    kept = sweep.pages_prune_count(cfgs, 4096, 4096, 4096, tg.F16)
+    assert 2 * len(cfgs) == 216 and 2 * kept == 214
+    assert sweep.PAGES_BUDGET == 228 * 1024
+
+
+def test_write_and_read_cache(tmp_path, monkeypatch):
+    import json
+
+    monkeypatch.setenv("TGEMM_CACHE_DIR", str(tmp_path))
+    monkeypatch.delenv("TGEMM_AUTOTUNE_DISABLE_CACHE", raising=False)
+    rows = [dict(block_M=128, block_N=128, block_K=32, num_stages=3, ok=True, median_ms=0.01, min_ms=0.009,
+                 smem_bytes=1000, smem_bound=900, tflops=1.0, extra="dropped"),
+            dict(block_M=128, block_N=64, block_K=32, num_stages=2, ok=False, error="x")]
+    sweep.write_cache("NVIDIA GB300", "wl", rows[0], rows)
+    assert sweep.load_cached("NVIDIA GB300", "wl") == rows[0]
+    lat = json.load(open(sweep.cache_path("NVIDIA GB300", "wl", "latency.json")))
+    assert len(lat) == 2 and "extra" not in lat[0] and lat[1]["ok"] is False
+    monkeypatch.setenv("TGEMM_AUTOTUNE_DISABLE_CACHE", "1")
+    assert sweep.load_cached("NVIDIA GB300", "wl") is None

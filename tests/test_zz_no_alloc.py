@@ -80,7 +80,7 @@ def test_noalloc_rejects_what_the_plan_rejects(cuda_lib):
     p = x.data_ptr()
     assert tg.tgemm_run_noalloc(4000, 3000, 5000, "f16", "f32", 256, 256, 64, 4, p, p, p)[0] == tg.ERR_SMEM_BUDGET
     assert tg.tgemm_run_noalloc(128, 128, 12, "f16", "f32", 128, 128, 32, 3, p, p, p)[0] == tg.ERR_ALIGNMENT
-    assert tg.tgemm_run_noalloc(128, 128, 64, "f16", "f32", 64, 128, 32, 3, p, p, p)[0] == tg.ERR_NO_KERNEL
+    assert tg.tgemm_run_noalloc(128, 128, 64, "f16", "f32", 96, 128, 32, 3, p, p, p)[0] == tg.ERR_NO_KERNEL
     assert tg.tgemm_run_noalloc(128, 128, 64, "f16", "f32", 128, 128, 32, 3, p + 2, p, p)[0] == tg.ERR_ALIGNMENT
     assert tg.tgemm_run_noalloc(0, 128, 64, "f16", "f32", 128, 128, 32, 3, 0, 0, 0) == (tg.OK, tg.OK)
 
