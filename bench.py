@@ -58,6 +58,8 @@ def parse_args(argv=None):
                     help="K splits reduced inside the kernel by clusters of this many CTAs (default: tuned table)")
     ap.add_argument("--stream-operands", type=int, choices=(0, 1), default=None,
                     help="1: L2 evict-first hint on the operand loads (default: tuned table)")
+    ap.add_argument("--grid-reduce", type=int, choices=(0, 1), default=None,
+                    help="1: reduce K splits inside the GEMM kernel after a grid-wide barrier (default: tuned table)")
     ap.add_argument("--group-m", type=int, default=None,
                     help="M-blocks per raster group of the persistent schedule (default: tuned table; 0 = 8)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -150,12 +152,13 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
-def config_key(block, stages, pair, split_k, group_m=8, cluster_k=0, stream_operands=False):
+def config_key(block, stages, pair, split_k, group_m=8, cluster_k=0, stream_operands=False, grid_reduce=False):
     """The launch configuration as the ncu summaries record it."""
     key = (f"{block[0]},{block[1]},{block[2]} S{stages} pair{int(bool(pair))} split{int(split_k)} "
            f"group{int(group_m) or 8}")
     key += f" cluster{int(cluster_k)}" if cluster_k and cluster_k > 1 else ""
-    return key + (" stream" if stream_operands else "")
+    key += " stream" if stream_operands else ""
+    return key + (" gridreduce" if grid_reduce else "")
 
 
 def recorded_traffic(workload, config=None):
@@ -367,6 +370,7 @@ def run_ours(args, w, world, rank, local):
         group_m = args.group_m or 0
         cluster_k = args.cluster_k or 0
         stream_ops = bool(args.stream_operands)
+        grid_red = bool(args.grid_reduce)
     else:
         cfg = tg.default_config(M, N, K, w["dtype"], w["out"])
         block, stages, pair, split_k = cfg["block"], cfg["num_stages"], cfg["cta_pair"], cfg["split_k"]
@@ -379,6 +383,7 @@ def run_ours(args, w, world, rank, local):
             split_k = args.split_k
         cluster_k = cfg["cluster_k"] if args.cluster_k is None else args.cluster_k
         stream_ops = cfg["stream_operands"] if args.stream_operands is None else bool(args.stream_operands)
+        grid_red = cfg["grid_reduce"] if args.grid_reduce is None else bool(args.grid_reduce)
     A, B = inputs.workload_operands(args.workload)
     hA = inputs.bits_to_torch(A, w["dtype"])
     hB = inputs.bits_to_torch(B, w["dtype"])
@@ -386,7 +391,7 @@ def run_ours(args, w, world, rank, local):
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[w["out"]]
     dC = torch.empty((M, N), dtype=tdt, device=dev)
     plan = tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k, group_m=group_m,
-                   cluster_k=cluster_k, stream_operands=stream_ops)
+                   cluster_k=cluster_k, stream_operands=stream_ops, grid_reduce=grid_red)
     info = plan.info
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -446,7 +451,8 @@ def run_ours(args, w, world, rank, local):
         pA, pB = hA.pin_memory(), hB.pin_memory()
         pCs = [torch.empty((M, N), dtype=tdt).pin_memory() for _ in range(2)]
         plans = [plan, tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k,
-                               group_m=group_m, cluster_k=cluster_k, stream_operands=stream_ops)]
+                               group_m=group_m, cluster_k=cluster_k, stream_operands=stream_ops,
+                               grid_reduce=grid_red)]
         bufs = [(dA, dB, dC), (torch.empty_like(dA), torch.empty_like(dB), torch.empty_like(dC))]
         streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
         torch.cuda.synchronize(dev)
@@ -497,12 +503,14 @@ def run_ours(args, w, world, rank, local):
         sustained.pop("_window", None)
 
     algo_bytes = (M * K + N * K) * 2 + M * N * (4 if w["out"] == "f32" else 2)
+    two_kernels = info["split_k"] > 1 and info["cluster_k"] <= 1 and not info["grid_reduce"]
     roofline = roofline_for(flops, algo_bytes, mean_ms / 1e3, measured_peaks())
     roofline.update({"traffic": recorded_traffic(args.workload,
                                                  config_key(block, stages, pair, info["split_k"], group_m,
-                                                            info["cluster_k"], info["stream_operands"])),
+                                                            info["cluster_k"], info["stream_operands"],
+                                                            info["grid_reduce"])),
                      "kernel": ("tgemm_kernel + splitk_reduce_kernel, timed together per step"
-                                if info["split_k"] > 1 and info["cluster_k"] <= 1 else "tgemm_kernel"),
+                                if two_kernels else "tgemm_kernel"),
                      "flops_per_launch": flops, "algorithmic_bytes_per_launch": algo_bytes})
 
     line = None
@@ -516,9 +524,10 @@ def run_ours(args, w, world, rank, local):
                 "config": dict(config_block(args, w, block, stages), cta_pair=int(pair),
                                split_k=int(info["split_k"]), group_m=int(group_m) or 8,
                                cluster_k=int(info["cluster_k"]),
-                               stream_operands=int(info["stream_operands"])), "roofline": roofline,
+                               stream_operands=int(info["stream_operands"]),
+                               grid_reduce=int(info["grid_reduce"])), "roofline": roofline,
                 "cpu_baseline": cpu,
-                "e2e": e2e, "gpu_launches": args.steps * (2 if info["split_k"] > 1 and info["cluster_k"] <= 1 else 1),
+                "e2e": e2e, "gpu_launches": args.steps * (2 if two_kernels else 1),
                 "clocks": clocks,
                 "sustained": sustained,
                 "plan": {k: info[k] for k in ("grid", "num_tiles", "smem_bytes", "tmem_columns", "acc_stages")},

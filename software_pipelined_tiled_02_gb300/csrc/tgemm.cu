@@ -101,6 +101,11 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     int *counters;              // outer > 1: [num_tiles][csk] arrival counts, zero between launches
     void *C;                    // the output, written with plain stores in mode 2
     int stream_ops;             // 1: operand loads carry an L2 evict-first hint
+    // K splits reduced inside the kernel after a grid-wide barrier (cooperative
+    // launch): grid_bar = {arrivals, generation}, zero between launches.
+    int grid_reduce;
+    uint32_t *grid_bar;
+    int out_mode_final;         // C's type (0 fp32, 1 fp16, 2 bf16); out_mode is what the tiles store
 };
 
 // ---------------------------------------------------------------- device side
@@ -331,6 +336,96 @@ __device__ __forceinline__ void mma_dispatch_nk(const Params &p, const MmaCtx &c
     case 2: mma_role<2, MH, PAIR>(p, c, abort, lane); break;
     case 4: mma_role<4, MH, PAIR>(p, c, abort, lane); break;
     default: mma_role<8, MH, PAIR>(p, c, abort, lane); break;
+    }
+}
+
+// K-split reduction inside the kernel (modes 0 and 1, grid_reduce).  The
+// launch is cooperative, so every CTA of the grid is resident at once and a
+// grid-wide barrier cannot wait forever for a CTA that has not started.
+// After its last unit, each CTA's epilogue has stored its fp32 partial tiles
+// to the workspace; thread 0 of the epilogue counts the CTA in, and the last
+// arrival opens the barrier by advancing its generation.  Then the epilogue
+// threads of all CTAs split the M x N outputs among themselves and add, for
+// each, its partials in split order 0, 1, ..., splits-1 -- the order of the
+// separate reduction kernel, so both give the same bits -- and round once to
+// C's type.  The barrier resets itself (arrivals back to 0), so launches need
+// no host-side state; its wait is bounded by the watchdog.
+__device__ __noinline__ void grid_reduce_phase(const Params &p, volatile int *abort, int *flag)
+{
+    const int et = int(threadIdx.x) - 2 * 32;  // 0..255 over the eight epilogue warps
+    if ((threadIdx.x & 31u) == 0) {
+        fence_proxy_async_global();  // this warp's completed partial stores, before the count below
+        __threadfence();
+    }
+    named_bar_sync(1, 8 * 32);
+    if (et == 0) {
+        uint32_t *count = p.grid_bar, *gen = p.grid_bar + 1;
+        const uint32_t g0 = ld_acquire_gpu(gen);
+        __threadfence();
+        if (atomicAdd(count, 1u) == gridDim.x - 1) {
+            *count = 0u;                 // the next launch starts from no arrivals
+            __threadfence();
+            st_release_gpu(gen, g0 + 1u);  // open the barrier
+        } else {
+            const uint64_t t0 = globaltimer();
+            uint32_t spins = 0;
+            while (ld_acquire_gpu(gen) == g0) {
+                if ((++spins & 63u) == 0 && globaltimer() - t0 > p.watchdog_ns) {
+                    report(p, kErrTimeout, 2, -1);
+                    *abort = 1;
+                    break;
+                }
+            }
+        }
+        *flag = *abort ? 0 : 1;
+    }
+    named_bar_sync(1, 8 * 32);
+    if (!*reinterpret_cast<volatile int *>(flag)) return;
+    __threadfence();
+    // Partial of split s at element e: ws[s * split_rows * N + e] (e < M * N;
+    // M * N and the split stride are multiples of 4).  A thread issues the
+    // loads of up to CH splits of its element, predicated rather than
+    // branched, before adding any of them.
+    constexpr int CH = 24;
+    const int64_t n4 = int64_t(p.M) * p.N / 4;
+    const int64_t stride4 = int64_t(p.split_rows) * p.N / 4;
+    const float4 *W = reinterpret_cast<const float4 *>(p.ws);
+    for (int64_t i = int64_t(blockIdx.x) * 256 + et; i < n4; i += int64_t(gridDim.x) * 256) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < p.splits; s0 += CH) {
+            float4 v[CH];
+#pragma unroll
+            for (int t = 0; t < CH; ++t)
+                if (s0 + t < p.splits) v[t] = __ldcg(W + int64_t(s0 + t) * stride4 + i);
+#pragma unroll
+            for (int t = 0; t < CH; ++t) {
+                if (s0 + t < p.splits) {
+                    if (s0 + t == 0) {
+                        acc = v[t];
+                    } else {
+                        acc.x += v[t].x;
+                        acc.y += v[t].y;
+                        acc.z += v[t].z;
+                        acc.w += v[t].w;
+                    }
+                }
+            }
+        }
+        if (p.out_mode_final == 0) {
+            reinterpret_cast<float4 *>(p.C)[i] = acc;
+        } else if (p.out_mode_final == 1) {
+            __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            reinterpret_cast<uint2 *>(p.C)[i] = u;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            reinterpret_cast<uint2 *>(p.C)[i] = u;
+        }
     }
 }
 
@@ -831,6 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
+        if (p.grid_reduce) grid_reduce_phase(p, abort, reinterpret_cast<int *>(smem + p.off_bar - 16));
     }
 
     tc_fence_before();
@@ -962,6 +1058,8 @@ struct tgemm_plan_s {
     int csk;                   // > 1: splits reduced inside the kernel by clusters of csk CTAs
     float *d_work;             // split-K partial sums: splits (or, with csk, splits / csk) x M x N fp32
     int *d_counters;           // csk with more than one cluster per tile: arrival counters
+    int grid_reduce;           // K splits reduced in the GEMM kernel after a grid-wide barrier
+    uint32_t *d_gbar;          // that barrier's arrival count and generation
     int *d_status;
     unsigned long long watchdog_ns;
     int debug_stall;
@@ -1112,6 +1210,7 @@ static int check_opts(const tgemm_plan_opts *opts, int num_stages)
         opts->cluster_k != 8)
         return kErrInvalidArg;
     if (opts->stream_operands != 0 && opts->stream_operands != 1) return kErrInvalidArg;
+    if (opts->grid_reduce != 0 && opts->grid_reduce != 1) return kErrInvalidArg;
     return kOk;
 }
 
@@ -1220,6 +1319,8 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     p->csk = csk;
     p->d_work = nullptr;
     p->d_counters = nullptr;
+    p->grid_reduce = splits > 1 && !csk && opts && opts->grid_reduce ? 1 : 0;
+    p->d_gbar = nullptr;
     p->device = dev;
     p->num_sms = sms;
     p->smem_limit = limit;
@@ -1306,6 +1407,17 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
             return kErrCuda;
         }
     }
+    if (p->grid_reduce) {
+        if (cudaMalloc(&p->d_gbar, 2 * sizeof(uint32_t)) != cudaSuccess ||
+            cudaMemset(p->d_gbar, 0, 2 * sizeof(uint32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            if (p->d_gbar) cudaFree(p->d_gbar);
+            if (p->d_work) cudaFree(p->d_work);
+            cudaFree(p->d_status);
+            delete p;
+            return kErrCuda;
+        }
+    }
     if (csk && outer > 1) {
         const size_t bytes = size_t(p->num_tiles) * size_t(csk) * sizeof(int);
         if (cudaMalloc(&p->d_counters, bytes) != cudaSuccess || cudaMemset(p->d_counters, 0, bytes) != cudaSuccess) {
@@ -1326,6 +1438,9 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     q.ws = p->d_work;
     q.counters = p->d_counters;
     q.stream_ops = opts && opts->stream_operands ? 1 : 0;
+    q.grid_reduce = p->grid_reduce;
+    q.grid_bar = p->d_gbar;
+    q.out_mode_final = out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
     *out = p;
     return kOk;
 }
@@ -1358,20 +1473,32 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
     if (rc != kOk) return rc;
     p->params.watchdog_ns = p->watchdog_ns;
     p->params.debug_stall = p->debug_stall;
-    if (p->pair || p->csk) {
+    if (p->pair || p->csk || p->grid_reduce) {
+        // Clusters for CTA pairs and the cluster reduction; a cooperative
+        // launch (every CTA resident at once) for the grid-wide reduction.
         cudaLaunchConfig_t cfg{};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = p->csk ? unsigned(p->csk) : 2u;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
+        cudaLaunchAttribute attr[2];
+        unsigned na = 0;
+        if (p->pair || p->csk) {
+            attr[na].id = cudaLaunchAttributeClusterDimension;
+            attr[na].val.clusterDim.x = p->csk ? unsigned(p->csk) : 2u;
+            attr[na].val.clusterDim.y = 1;
+            attr[na].val.clusterDim.z = 1;
+            ++na;
+        }
+        if (p->grid_reduce) {
+            attr[na].id = cudaLaunchAttributeCooperative;
+            attr[na].val.cooperative = 1;
+            ++na;
+        }
         cfg.gridDim = dim3(unsigned(p->grid), 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = size_t(p->smem_launch);
         cfg.stream = reinterpret_cast<cudaStream_t>(stream);
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, p->csk ? tgemm_kernel<2> : tgemm_kernel<1>, p->params) != cudaSuccess) {
+        cfg.numAttrs = na;
+        if (cudaLaunchKernelEx(&cfg, p->csk ? tgemm_kernel<2> : p->pair ? tgemm_kernel<1> : tgemm_kernel<0>,
+                               p->params) != cudaSuccess) {
             cudaGetLastError();
             return kErrCuda;
         }
@@ -1379,7 +1506,7 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
         tgemm_kernel<0><<<p->grid, kThreads, p->smem_launch, reinterpret_cast<cudaStream_t>(stream)>>>(p->params);
         if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     }
-    if (p->splits > 1 && !p->csk) {
+    if (p->splits > 1 && !p->csk && !p->grid_reduce) {
         const int64_t mn = p->M * p->N;
         const int64_t n4 = mn / 4;
         int blocks = int((n4 + 255) / 256);
@@ -1431,8 +1558,10 @@ int tgemm_status(tgemm_plan_t p, int *detail)
     }
     // A launch that gave up may have left some of the in-kernel split
     // reduction's arrival counters part-way: clear them for the next launch.
-    if (h[0] != kOk && p->d_counters &&
-        cudaMemset(p->d_counters, 0, size_t(p->num_tiles) * size_t(p->csk) * sizeof(int)) != cudaSuccess) {
+    if (h[0] != kOk && ((p->d_counters &&
+                         cudaMemset(p->d_counters, 0, size_t(p->num_tiles) * size_t(p->csk) * sizeof(int)) !=
+                             cudaSuccess) ||
+                        (p->d_gbar && cudaMemset(p->d_gbar, 0, 2 * sizeof(uint32_t)) != cudaSuccess))) {
         cudaGetLastError();
         return -kErrCuda;
     }
@@ -1484,6 +1613,7 @@ int tgemm_get_plan_info(tgemm_plan_t p, tgemm_plan_info *info)
     info->num_units = p->params.num_units;
     info->cluster_k = p->csk;
     info->stream_operands = p->params.stream_ops;
+    info->grid_reduce = p->grid_reduce;
     return kOk;
 }
 
@@ -1500,6 +1630,10 @@ int tgemm_destroy(tgemm_plan_t p)
         rc = kErrCuda;
     }
     if (p->d_counters && cudaFree(p->d_counters) != cudaSuccess) {
+        cudaGetLastError();
+        rc = kErrCuda;
+    }
+    if (p->d_gbar && cudaFree(p->d_gbar) != cudaSuccess) {
         cudaGetLastError();
         rc = kErrCuda;
     }

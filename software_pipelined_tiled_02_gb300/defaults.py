@@ -16,8 +16,9 @@ from __future__ import annotations
 # f16, 1 bf16, 2 f32.  Keys left out take their defaults (DEFAULT_OPTS):
 # cta_pair, split_k (K splits), group_m (the persistent raster's group of
 # M-blocks; 0: the library's 8), cluster_k (> 1: K splits reduced inside the
-# kernel by clusters of that many CTAs) and stream_operands (L2 evict-first
-# hint on the operand loads).  The comments give same-GPU, interleaved timings
+# kernel by clusters of that many CTAs), stream_operands (L2 evict-first
+# hint on the operand loads) and grid_reduce (K splits reduced in the GEMM
+# kernel after a grid-wide barrier).  The comments give same-GPU, interleaved timings
 # against the runner-up.
 FROZEN = {
     # 1643 vs 1607 TFLOP/s for one CTA 256x224x64, group 8
@@ -27,13 +28,14 @@ FROZEN = {
     # 94.2 vs 96.3 us without the evict-first hint; 96.3 vs 100.1 for 256x224x64 S6
     (4000, 3000, 5000, 0, 2): dict(block=(256, 384, 64), num_stages=4, cta_pair=True, stream_operands=True),
     # 31.2 vs 33.3 us without the evict-first hint; 35.4 for 128x128x64 S6 split 9; 166 unsplit;
-    # the in-kernel cluster reduction (128x256x64 S4, split 16, clusters of 4) 38.9
+    # the in-kernel cluster reduction (128x256x64 S4, split 16, clusters of 4) 38.9;
+    # the reduction in the GEMM kernel after a grid-wide barrier 33.3
     (512, 512, 32768, 0, 2): dict(block=(256, 256, 128), num_stages=3, cta_pair=True, split_k=19,
                                   stream_operands=True),
     (128, 128, 128, 0, 2): dict(block=(128, 128, 32), num_stages=3),
 }
 
-DEFAULT_OPTS = dict(cta_pair=False, split_k=1, group_m=0, cluster_k=0, stream_operands=False)
+DEFAULT_OPTS = dict(cta_pair=False, split_k=1, group_m=0, cluster_k=0, stream_operands=False, grid_reduce=False)
 
 # Candidate tiles: (block, depth, relative steady-state throughput per SM
 # measured at full waves on GB300 with one CTA 256x256 = 1, CTA pair).  A

@@ -141,7 +141,7 @@ def write_cache(device_name: str, workload: str, best: dict, rows: list):
     """best_config.json (the winner) and latency.json (every candidate)."""
     os.makedirs(cache_dir(device_name, workload), exist_ok=True)
     keys = ("block_M", "block_N", "block_K", "num_stages", "cta_pair", "split_k", "cluster_k", "stream_operands",
-            "prefetch", "median_ms", "min_ms", "tflops", "smem_bytes", "smem_bound", "ok", "worst_error_ratio",
+            "grid_reduce", "prefetch", "median_ms", "min_ms", "tflops", "smem_bytes", "smem_bound", "ok", "worst_error_ratio",
             "error")
     lat = [{k: r[k] for k in keys if k in r} for r in rows]
     for name, obj in (("best_config.json", best), ("latency.json", lat)):
@@ -187,7 +187,8 @@ class Runner:
             plan = tg.Plan(self.M, self.N, self.K, w["dtype"], w["out"],
                            (c["block_M"], c["block_N"], c["block_K"]), c["num_stages"], pair=bool(c.get("cta_pair")),
                            prefetch=int(c.get("prefetch", 0)), split_k=int(c.get("split_k", 1) or 1),
-                           cluster_k=int(c.get("cluster_k", 0)), stream_operands=bool(c.get("stream_operands")))
+                           cluster_k=int(c.get("cluster_k", 0)), stream_operands=bool(c.get("stream_operands")),
+                           grid_reduce=bool(c.get("grid_reduce")))
         except tg.TgemmError as e:
             row.update(ok=False, error=str(e))
             return row

@@ -48,7 +48,7 @@ C_PROGRAM = r"""
 
 int main(void)
 {
-    tgemm_plan_opts opts = {1, 2, 1, 0, 0, 0};  /* cta_pair, group_m, split_k, prefetch, cluster_k, stream */
+    tgemm_plan_opts opts = {1, 2, 1, 0, 0, 0, 0};  /* cta_pair, group_m, split_k, prefetch, cluster_k, stream, grid_reduce */
     int64_t bound = tgemm_smem_bound(TGEMM_F16, 128, 128, 32, 3);
     int one = tgemm_validate(4096, 4096, 4096, TGEMM_F16, TGEMM_F16, 256, 224, 64, 3, 232448);
     int pair = tgemm_validate_ex(4096, 4096, 4096, TGEMM_F16, TGEMM_F16, 256, 224, 128, 3, 232448, &opts);
@@ -194,10 +194,11 @@ def test_validate_ex_options(lib):
     assert V(M, 4, 2 * 32, tg.F16, tg.F32, 128, 32, 32, 4, L, split_k=64) == tg.OK
 
 
-def test_validate_ex_stream_operands(lib):
+def test_validate_ex_stream_operands_and_grid_reduce(lib):
     V = tg.tgemm_validate_ex
     for v, want in ((0, tg.OK), (1, tg.OK), (2, tg.ERR_INVALID_ARG), (-1, tg.ERR_INVALID_ARG)):
         assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, LIMIT_227K, stream_operands=v) == want
+        assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, LIMIT_227K, split_k=4, grid_reduce=v) == want
 
 
 def test_validate_ex_cluster_k_rules(lib):

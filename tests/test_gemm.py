@@ -484,3 +484,33 @@ def test_cluster_split_long_k_full_and_integer(cuda_lib):
             assert np.array_equal(C, R)
         else:
             assert_close(C, R, S, w["out"])
+
+
+@pytest.mark.parametrize("block,stages,pair,split_k,shape", [
+    ((256, 256, 128), 3, True, 19, (512, 512, 32768)),   # the long-K default
+    ((128, 128, 64), 4, False, 5, (300, 520, 2056)),     # one CTA, ragged M, persistent with several units per CTA
+    ((256, 224, 64), 3, True, 3, (1000, 1040, 4104)),    # more units than pairs
+    ((64, 256, 32), 2, False, 64, (129, 264, 8192)),     # the most splits, M = 64 tiles
+])
+@pytest.mark.parametrize("out", ["f32", "f16"])
+def test_in_kernel_split_reduction_equals_second_kernel(cuda_lib, block, stages, pair, split_k, shape, out):
+    # The grid-wide reduction inside the GEMM kernel adds the partials in the
+    # same order as the separate reduction kernel: the same bits, launch after
+    # launch (its barrier resets itself), and within the oracle's tolerance.
+    M, N, K = shape
+    A, B = inputs.operands(91 + split_k, M, N, K, "f16", "uniform")
+    dA, dB = to_dev(A, "f16"), to_dev(B, "f16")
+    res = []
+    for gr in (True, False):
+        plan = cuda_lib.Plan(M, N, K, "f16", out, block, stages, pair=pair, split_k=split_k, grid_reduce=gr)
+        assert plan.info["grid_reduce"] == int(gr) and plan.info["split_k"] > 1
+        for _ in range(3 if gr else 1):
+            res.append(plan.run(dA, dB))
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+        plan.close()
+    for C in res[1:]:
+        assert torch.equal(C.view(torch.int32 if out == "f32" else torch.int16),
+                           res[0].view(torch.int32 if out == "f32" else torch.int16))
+    R, S = oracle.gemm(A, B, "f16")
+    assert_close(as_f64(res[0]), R, S, out)
