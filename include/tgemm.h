@@ -103,8 +103,7 @@ int tgemm_smem_limit(void);
  *   - K % 8 == 0, N * out_bytes % 16 == 0 (row pitch)      -> ALIGNMENT
  *   - block_M in {64, 128, 256} (64: M = 64 tensor-core
  *     instructions; cta_pair: 256 only); block_N a multiple
- *     of 32 in [32, 256] (with cta_pair also 320, 384, 448,
- *     512);
+ *     of 32 in [32, 256] (with cta_pair up to 512);
  *     block_K in {16, 32, 64, 128} (16-bit
  *     operands: rows of 32, 64 or 128 bytes, or two 128-byte
  *     K-panels for 128)                                     -> NO_KERNEL
@@ -139,8 +138,8 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
  *     block_M = 256 tile: one M = 256 tensor-core instruction per K step spans
  *     both SMs, each CTA holds 128 rows of A, block_N / 2 rows of B and 128
  *     rows of the accumulator.  Only block_M = 256 is accepted.  block_N may
- *     then also be 320, 384, 448 or 512: two N = block_N / 2 instructions per K
- *     step share the A operand (each SM pulls less operand data per FLOP, but
+ *     then also be a multiple of 32 from 288 to 512: two N = block_N / 2
+ *     instructions per K step share the A operand (each SM pulls less operand data per FLOP, but
  *     the accumulator fills tensor memory, so the epilogue of a tile no longer
  *     overlaps the next tile's K loop).  Each CTA is a
  *     block in the sense of the pages' budget rule: the bound checked is

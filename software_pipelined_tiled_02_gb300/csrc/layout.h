@@ -63,14 +63,16 @@ inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 // 128-byte spans (block_K = 128 for 16-bit operands: the slot then holds two
 // K-panels of 64 elements, each a standard 128-byte-swizzled tile).  The
 // CTA-pair mode implements only block_M = 256 (one M = 256 MMA over the two
-// CTAs' 128-row halves), and also tiles of 320 to 512 columns in steps of 64:
-// two MMAs of N = block_N / 2 per k-step that share the A operand, so each SM
-// pulls a quarter less operand data per FLOP than with 256 columns.
+// CTAs' 128-row halves), and also tiles of 288 to 512 columns in steps of 32:
+// two MMAs of N = block_N / 2 (a multiple of 16) per k-step that share the A
+// operand, so each SM pulls up to a quarter less operand data per FLOP than
+// with 256 columns.  Each CTA then holds block_N / 4 rows of each N-half of B,
+// a whole number of 8-row swizzle atoms.
 inline bool tile_supported(int bm, int bn, int bk, int in_bytes, int pair = 0)
 {
     if (pair && bm != 256) return false;
     if (bm != 64 && bm != 128 && bm != 256) return false;
-    const bool wide = pair && bn > 256 && bn <= 512 && bn % 64 == 0;
+    const bool wide = pair && bn > 256 && bn <= 512 && bn % 32 == 0;
     if (!wide && (bn < 32 || bn > 256 || bn % 32 != 0)) return false;
     int row = bk * in_bytes;
     return (row == 32 || row == 64 || row == 128 || row == 256) && bk > 0;

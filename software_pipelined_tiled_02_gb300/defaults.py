@@ -25,8 +25,9 @@ FROZEN = {
     (4096, 4096, 4096, 0, 0): dict(block=(256, 224, 128), num_stages=3, cta_pair=True, group_m=2),
     # 1753 vs 1692 for one CTA 256x256x64
     (8192, 8192, 8192, 1, 1): dict(block=(256, 256, 128), num_stages=3, cta_pair=True),
-    # 94.2 vs 96.3 us without the evict-first hint; 96.3 vs 100.1 for 256x224x64 S6
-    (4000, 3000, 5000, 0, 2): dict(block=(256, 384, 64), num_stages=4, cta_pair=True, stream_operands=True),
+    # 144 tiles of 256x352 fill two waves of 76 pairs: 91.8-92.4 us vs 92.6-93.8 for 256x384x64 S4
+    # (128 tiles); 94.2 vs 96.3 us with and without the evict-first hint; 100.1 for 256x224x64 S6
+    (4000, 3000, 5000, 0, 2): dict(block=(256, 352, 64), num_stages=5, cta_pair=True, stream_operands=True),
     # 31.2 vs 33.3 us without the evict-first hint; 35.4 for 128x128x64 S6 split 9; 166 unsplit;
     # the in-kernel cluster reduction (128x256x64 S4, split 16, clusters of 4) 38.9;
     # the reduction in the GEMM kernel after a grid-wide barrier 33.3
@@ -43,6 +44,7 @@ DEFAULT_OPTS = dict(cta_pair=False, split_k=1, group_m=0, cluster_k=0, stream_op
 CANDIDATES = (
     ((256, 256, 128), 3, 1.04, True),
     ((256, 384, 64), 4, 1.04, True),   # two N = 192 MMAs per k-step; measured on 4000x3000x5000
+    ((256, 352, 64), 5, 1.04, True),   # two N = 176 MMAs per k-step
     ((256, 224, 64), 5, 1.00, True),
     ((256, 256, 64), 3, 1.00, False),
     ((256, 224, 64), 3, 0.98, False),

@@ -51,7 +51,7 @@ import software_pipelined_tiled_02_gb300 as tg  # noqa: E402
 from software_pipelined_tiled_02_gb300 import inputs  # noqa: E402
 
 PAGES_SPACE = dict(block_M=(64, 128, 256), block_N=(64, 128, 256), block_K=(16, 32, 64), num_stages=(1, 2, 3, 4))
-GB300_SPACE = dict(block_M=(128, 256), block_N=(64, 128, 192, 224, 256, 384, 512), block_K=(32, 64, 128),
+GB300_SPACE = dict(block_M=(128, 256), block_N=(64, 128, 192, 224, 256, 352, 384, 512), block_K=(32, 64, 128),
                    num_stages=(2, 3, 4, 5, 6, 8), cta_pair=(0, 1))
 
 

@@ -102,6 +102,8 @@ def test_integer_inputs_bit_exact(cuda_lib, block, stages, dtype):
 PAIR_CONFIGS = [
     ((256, 512, 64), 4),     # two N = 256 MMAs per k-step sharing A
     ((256, 384, 128), 2),    # two N = 192 MMAs, two K-panels per slot
+    ((256, 352, 64), 4),     # two N = 176 MMAs: 88 B rows per CTA and N-half
+    ((256, 288, 32), 5),     # two N = 144 MMAs
     ((256, 256, 128), 3),
     ((256, 224, 128), 3),
     ((256, 256, 64), 4),

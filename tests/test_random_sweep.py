@@ -24,7 +24,8 @@ SINGLE_TILES = [(128, 128, 32), (128, 256, 64), (256, 128, 64), (128, 64, 16), (
                 (256, 96, 128), (128, 32, 64), (256, 256, 64), (128, 192, 64), (64, 128, 32), (64, 256, 64),
                 (64, 64, 128)]
 PAIR_TILES = [(256, 256, 128), (256, 224, 128), (256, 256, 64), (256, 128, 32), (256, 64, 16), (256, 32, 64),
-              (256, 192, 128), (256, 160, 64), (256, 512, 64), (256, 448, 128), (256, 384, 64), (256, 320, 32)]
+              (256, 192, 128), (256, 160, 64), (256, 512, 64), (256, 448, 128), (256, 384, 64), (256, 320, 32),
+              (256, 352, 64), (256, 416, 128), (256, 480, 32)]
 N_CASES = int(os.environ.get("TGEMM_SWEEP_CASES", "400"))  # more for a longer soak
 SEED = int(os.environ.get("TGEMM_SWEEP_SEED", "20261202"))   # another seed draws other cases
 

@@ -79,6 +79,7 @@ def test_bit_identical_across_stages_4096(cuda_lib):
 
 @pytest.mark.parametrize("block,stage_list", [((256, 256, 64), (1, 2, 4, 6)), ((256, 128, 32), (1, 3, 8)),
                                               ((256, 224, 128), (1, 2, 3)), ((256, 512, 64), (1, 2, 4)),
+                                              ((256, 352, 64), (1, 2, 4)),
                                               ((256, 448, 128), (1, 2))])
 def test_bit_identical_across_stages_pair(cuda_lib, block, stage_list):
     res = outputs_over_stages(cuda_lib, 1000, 1040, 2056, "bf16", "f32", block, stage_list, seed=78, pair=True)
