@@ -516,3 +516,40 @@ def test_in_kernel_split_reduction_equals_second_kernel(cuda_lib, block, stages,
                            res[0].view(torch.int32 if out == "f32" else torch.int16))
     R, S = oracle.gemm(A, B, "f16")
     assert_close(as_f64(res[0]), R, S, out)
+
+
+def test_gemm_from_several_host_threads(cuda_lib):
+    # gemm() holds its plan cache's lock for the lookup only and each plan's own
+    # lock for the enqueue: threads on different plans run side by side, and
+    # threads sharing a plan take turns.  Every result must still be right.
+    import threading
+
+    shapes = [(256, 512, 1024), (384, 256, 512), (256, 512, 1024), (512, 768, 256)]
+    work = []
+    for i, (M, N, K) in enumerate(shapes):
+        A, B = inputs.operands(700 + i, M, N, K, "f16", "uniform")
+        work.append((A, B, to_dev(A, "f16"), to_dev(B, "f16")))
+    results, errors = [None] * len(work), []
+
+    def worker(i):
+        try:
+            _, _, dA, dB = work[i]
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                outs = [cuda_lib.gemm(dA, dB, out_dtype=torch.float32, stream=stream) for _ in range(20)]
+            stream.synchronize()
+            results[i] = outs
+        except Exception as e:  # reported below, in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(work))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for (A, B, _, _), outs in zip(work, results):
+        R, S = oracle.gemm(A, B, "f16")
+        for C in outs:
+            assert torch.equal(C, outs[0])
+        assert_close(as_f64(outs[0]), R, S, "f32")
