@@ -22,14 +22,20 @@ pytestmark = pytest.mark.gpu
 
 TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 
-# (block, num_stages, cta_pair, split_k): one CTA, pairs with one and two
-# K-panels per slot, and the split-K path whose partials meet in the reduction
+# (block, num_stages, cta_pair, split_k, options): one CTA (64- and 128-row
+# tiles), pairs with one and two K-panels per slot and a wide tile, and the
+# split-K paths whose partials meet in the second kernel, in the GEMM kernel
+# after a grid-wide barrier, or in a cluster through distributed shared memory
 CONFIGS = [
-    ((128, 128, 32), 3, False, 1),
-    ((256, 224, 64), 6, True, 1),
-    ((256, 224, 128), 3, True, 1),
-    ((256, 256, 128), 3, True, 3),
-    ((128, 128, 64), 4, False, 2),
+    ((128, 128, 32), 3, False, 1, {}),
+    ((64, 128, 64), 4, False, 1, {}),
+    ((256, 224, 64), 6, True, 1, {}),
+    ((256, 224, 128), 3, True, 1, {"stream_operands": True}),
+    ((256, 352, 64), 4, True, 1, {}),
+    ((256, 256, 128), 3, True, 3, {}),
+    ((128, 128, 64), 4, False, 2, {}),
+    ((256, 256, 64), 3, True, 3, {"grid_reduce": True}),
+    ((128, 256, 64), 3, False, 6, {"cluster_k": 2}),
 ]
 
 
@@ -59,12 +65,12 @@ def reference(At, Bt, out):
     return torch.from_numpy(R).to(TORCH[out])
 
 
-@pytest.mark.parametrize("block,stages,pair,split", CONFIGS, ids=lambda v: str(v))
+@pytest.mark.parametrize("block,stages,pair,split,opts", CONFIGS, ids=lambda v: str(v))
 @pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("f16", "f16"), ("bf16", "bf16")])
-def test_nan_and_inf_follow_ieee(cuda_lib, block, stages, pair, split, dtype, out):
+def test_nan_and_inf_follow_ieee(cuda_lib, block, stages, pair, split, opts, dtype, out):
     M, N, K = 300, 264, 384  # 16-bit C rows must be whole 16-byte units
     At, Bt = operands_with_specials(dtype, M, N, K)
-    plan = cuda_lib.Plan(M, N, K, dtype, out, block, stages, pair=pair, split_k=split)
+    plan = cuda_lib.Plan(M, N, K, dtype, out, block, stages, pair=pair, split_k=split, **opts)
     C = torch.full((M, N), 5.0, dtype=TORCH[out], device="cuda")
     plan.run(At.cuda(), Bt.cuda(), C)
     torch.cuda.synchronize()
