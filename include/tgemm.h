@@ -189,6 +189,25 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
  *     the same time (long K over few tiles); it costs where tiles of later
  *     waves read the same rows again (large square problems).  Results do not
  *     depend on it.  Other values: INVALID_ARG.
+ *   stream_k: 0 = every tile is one persistent work unit.  1 = when the tiles
+ *     do not fill the last wave of workers (CTAs, or CTA pairs), the tiles
+ *     past the last whole wave are shared out by k-blocks: each worker takes
+ *     an equal contiguous run of the tail's k-block iterations, tile after
+ *     tile, so all workers finish together.  A tile covered by several runs is
+ *     finished by the last of them to complete: each run stores its fp32
+ *     partial to a workspace the plan allocates (workers x 2 x block_M x
+ *     block_N floats) and counts in; the last adds the runs' partials in k
+ *     order and writes C.  No CTA waits for another.  Sums stay in a fixed
+ *     order (a function of the shape, the tile and the number of workers),
+ *     so results are bit-identical across num_stages.  Not combined with
+ *     split_k > 1 or cluster_k > 1 (INVALID_ARG).  Left off (no tail) when the
+ *     tiles fill whole waves or the tail has fewer than two k-blocks per
+ *     worker.  Launches of one such plan must be ordered.  On GB300 it does
+ *     not pay yet: each lane of the epilogue holds one row, so the pieces'
+ *     fp32 stores and the finishing loads touch 32 rows per instruction, and
+ *     that traffic costs more than the idle tail it removes (8192^3 bf16:
+ *     614 us against 598 us without it; 588 us with the piece traffic
+ *     switched off in a probe).
  *   grid_reduce: with split_k > 1 and cluster_k <= 1: 0 = a second kernel
  *     reduces the K splits; 1 = the GEMM kernel does, after a grid-wide
  *     barrier.  The launch is then cooperative, so every CTA of the
@@ -206,12 +225,13 @@ typedef struct tgemm_plan_opts {
     int cluster_k;
     int stream_operands;
     int grid_reduce;
+    int stream_k;
 } tgemm_plan_opts;
 
 /* tgemm_validate with options (NULL = defaults): the option ranges above
  * (cta_pair 0 or 1, group_m 0..4096, split_k 0..64, prefetch 0..num_stages,
- * cluster_k 0, 1, 2, 4 or 8, stream_operands and grid_reduce 0 or 1) give
- * INVALID_ARG, then the checks of
+ * cluster_k 0, 1, 2, 4 or 8, stream_operands, grid_reduce and stream_k 0 or 1;
+ * stream_k with split_k > 1 or cluster_k > 1) give INVALID_ARG, then the checks of
  * tgemm_validate, the split-K workspace rule and the cluster_k rules, as
  * tgemm_plan_ex makes them. */
 int tgemm_validate_ex(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M,
@@ -291,6 +311,7 @@ typedef struct tgemm_plan_info {
     int cluster_k;       /* > 1: K splits reduced in the kernel by clusters of this many CTAs */
     int stream_operands; /* 1: operand loads carry an L2 evict-first hint */
     int grid_reduce;     /* 1: K splits reduced in the GEMM kernel after a grid-wide barrier */
+    int stream_k_tiles;  /* tiles of the stream-K tail (0: none) */
 } tgemm_plan_info;
 
 int tgemm_get_plan_info(tgemm_plan_t plan, tgemm_plan_info *info);

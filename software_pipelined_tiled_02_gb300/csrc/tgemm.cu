@@ -106,6 +106,13 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     int grid_reduce;
     uint32_t *grid_bar;
     int out_mode_final;         // C's type (0 fp32, 1 fp16, 2 bf16); out_mode is what the tiles store
+    // Persistent schedule: `workers` CTAs (or pairs) take work units round robin:
+    // units 0 .. dp_units-1 whole.  With a stream-K tail, the last sk_tiles
+    // tiles' k-blocks are shared out as equal contiguous runs, one per worker.
+    int workers, dp_units, sk_tiles;
+    int sk_rows;                // rows of a tile one CTA holds (its part of a stream-K partial)
+    float *sk_ws;               // [workers][2][ranks][sk_rows][bn] fp32 partial pieces
+    int *sk_cnt;                // [sk_tiles][ranks] arrival counts, zero between launches
 };
 
 // ---------------------------------------------------------------- device side
@@ -190,6 +197,8 @@ __device__ __forceinline__ void tile_coords(const Params &p, int t, int &m_blk, 
 // partial-sum workspace, R = tiles_m * block_M >= M; 0 without splitting).
 struct Unit {
     int mb, nb, kb0, kb1, row_off;
+    int sk;       // 1: a piece of a stream-K tile (k-blocks kb0 .. kb1-1 of it)
+    int sk_tile;  // that tile's index among the stream-K tiles
 };
 
 __device__ __forceinline__ Unit unit_coords(const Params &p, int u)
@@ -202,6 +211,51 @@ __device__ __forceinline__ Unit unit_coords(const Params &p, int u)
     w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
     w.row_off = split * p.split_rows;
     return w;
+}
+
+// Stream-K tail.  The tail's tiles have sk_tiles x num_kb k-block iterations
+// in all, tile by tile; worker w takes iterations [I*w/W, I*(w+1)/W), fewer
+// than one tile's worth, so at most two tiles.  Tile t's pieces belong to the
+// workers sk_lo(t) .. sk_hi(t), in k order.
+__device__ __forceinline__ int64_t sk_start(const Params &p, int w)
+{
+    return int64_t(p.sk_tiles) * p.num_kb * w / p.workers;
+}
+__device__ __forceinline__ int sk_lo(const Params &p, int t)
+{
+    const int64_t I = int64_t(p.sk_tiles) * p.num_kb;
+    return int((int64_t(p.workers) * (int64_t(t) * p.num_kb + 1) + I - 1) / I) - 1;
+}
+__device__ __forceinline__ int sk_hi(const Params &p, int t)
+{
+    const int64_t I = int64_t(p.sk_tiles) * p.num_kb;
+    return int((int64_t(p.workers) * (int64_t(t + 1) * p.num_kb) + I - 1) / I) - 1;
+}
+
+// Work item i of worker w (a CTA, or a CTA pair): false once w has no more.
+// Whole units come first (round robin over the workers), then w's stream-K
+// pieces.  Every role of a CTA walks the same items in the same order.
+__device__ __forceinline__ bool work_item(const Params &p, int w, int i, Unit &u)
+{
+    const int n_whole = w < p.dp_units ? (p.dp_units - w + p.workers - 1) / p.workers : 0;
+    if (i < n_whole) {
+        u = unit_coords(p, w + i * p.workers);
+        u.sk = 0;
+        u.sk_tile = 0;
+        return true;
+    }
+    if (p.sk_tiles == 0) return false;
+    const int64_t s0 = sk_start(p, w), s1 = sk_start(p, w + 1);
+    const int t = int(s0 / p.num_kb) + (i - n_whole);
+    if (i - n_whole > 1 || int64_t(t) * p.num_kb >= s1) return false;
+    const int64_t base = int64_t(t) * p.num_kb;
+    u.kb0 = int((s0 > base ? s0 : base) - base);
+    u.kb1 = int((s1 < base + p.num_kb ? s1 : base + p.num_kb) - base);
+    tile_coords(p, p.dp_units + t, u.mb, u.nb);
+    u.row_off = 0;
+    u.sk = 1;
+    u.sk_tile = t;
+    return true;
 }
 
 // Shared-memory matrix descriptor of a K-major swizzled operand tile starting
@@ -261,9 +315,10 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
     int it = 0;
     bool ok = true;
     if (p.debug_stall) ok = warp_wait(c.stall, 0, p, abort, 1, 0);  // test hook: nothing arrives
-    for (int t = c.unit0; ok && t < p.num_units; t += c.ustride) {
-        const int kb0 = (t - (t / p.splits) * p.splits) * p.kb_per_split;
-        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+    for (int i = 0; ok; ++i) {
+        Unit w;
+        if (!work_item(p, c.unit0, i, w)) break;
+        const int kb0 = w.kb0, kb1 = w.kb1;
         if (!warp_wait(acc_empty(a), aph ^ 1u, p, abort, 1, it)) break;
         tc_fence_after();
         const uint32_t d = c.tmem + uint32_t(a * p.acc_cols);
@@ -647,8 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
     auto acc_empty = [&](int a) { return bars + 8u * uint32_t(2 * S + 2 + a); };
     const uint32_t drain = bars + 8u * uint32_t(2 * S + 4);
     const uint32_t stall = bars + 8u * uint32_t(2 * S + 5);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bar + 8u * uint32_t(2 * S + 6));
+    const uint32_t epi_bar = bars + 8u * uint32_t(2 * S + 6);  // the eight epilogue warps meet here
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bar + 8u * uint32_t(2 * S + 7));
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *flag = reinterpret_cast<int *>(tmem_slot + 2);  // "counted in last", for the epilogue warps
 
     const int warp = int(threadIdx.x) / 32;
     const int lane = int(threadIdx.x) % 32;
@@ -667,6 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         }
         mbar_init(drain, 1);
         mbar_init(stall, 1);
+        mbar_init(epi_bar, kEpiWarps);
         *abort = 0;
         fence_mbar_init();
         if (p.num_kb > 0) {
@@ -710,8 +768,9 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         const int D = p.prefetch;
         int sd = S - D;  // slot of iteration issued - D, once issued >= D
         uint32_t phd = 0;
-        for (int t = unit0; ok && t < p.num_units; t += ustride) {
-            const Unit w = unit_coords(p, t);
+        for (int i = 0; ok; ++i) {
+            Unit w;
+            if (!work_item(p, unit0, i, w)) break;
             const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn + int(rank) * p.b_box_rows;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 if (!warp_wait(empty(s), ph ^ 1u, p, abort, 0, issued)) {
@@ -836,78 +895,177 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         uint32_t aph = 0;
         uint32_t chunk = 0;
         int tiles_done = 0;
-        for (int t = unit0; t < p.num_units; t += ustride, ++tiles_done) {
-            const Unit w = unit_coords(p, t);
+        constexpr int kRanks = PAIR ? 2 : 1;
+        // The epilogue warps meet on epi_bar, one arrival per warp.  The wait is
+        // bounded: a warp that left the loop on an abort turns into a recorded
+        // timeout for the others, never a hang.
+        uint32_t epi_ph = 0;
+        auto epi_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_bar);
+            const bool met = warp_wait(epi_bar, epi_ph, p, abort, 2, tiles_done, false);
+            epi_ph ^= 1u;
+            return met;
+        };
+        bool sk_ok = true;
+        for (int i = 0;; ++i, ++tiles_done) {
+            Unit w;
+            if (!work_item(p, unit0, i, w)) break;
             const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn;
             if (!warp_wait(acc_full(a), aph, p, abort, 2, tiles_done)) break;
             tc_fence_after();
-            int idx = 0;
-            for (int h = 0; h < p.m_halves; ++h) {
-                // this warp's accumulator rows: quarter_rows of them, from TMEM lane 32q;
-                // with 16 rows (M = 64) lanes 16-31 load and stage values the store leaves out
-                const int row0 = m0 + h * 128 + q * p.quarter_rows;
-                if (row0 >= p.M) continue;  // warp-uniform
-                for (int c = 0; c * kEpiCols < p.bn; ++c) {
-                    const int col0 = n0 + c * kEpiCols;
-                    if (col0 >= p.N) break;  // warp-uniform
-                    if ((idx++ & 1) != sub) continue;  // the other warp of this quarter takes it
-                    // the chunk's TMEM columns, staging buffer and store box lie inside their regions
-                    if (!check(a * p.acc_cols + h * p.bn + (c + 1) * kEpiCols <= p.tmem_cols &&
-                                   uint32_t((warp - 1) * nbuf) * p.c_buf_bytes <= p.off_bar - p.off_c &&
-                                   col0 % 8 == 0 && w.row_off + row0 >= 0,
-                               p, abort, 2, tiles_done))
-                        continue;
-                    uint32_t v[32];
-                    if (p.num_kb > 0) {
-                        tmem_ld_32x32b_x32(tmem + lane_base + uint32_t(a * p.acc_cols + h * p.bn + c * kEpiCols), v);
-                        tmem_wait_ld();
-                    } else {
+            // A stream-K piece that is not its whole tile: every piece of the tile
+            // stores its fp32 partial (pass 1) and counts in; the last to count adds
+            // all the tile's pieces in k order (pass 2) and writes C.
+            const bool piece = w.sk && !(w.kb0 == 0 && w.kb1 == p.num_kb);
+            const int lo = piece ? sk_lo(p, w.sk_tile) : 0;
+            const int hi = piece ? sk_hi(p, w.sk_tile) : -1;
+            // Piece of worker v in stream-K tile t: workspace slot 2v + (t - first tile of v).
+            auto piece_at = [&](int v, int r, int col) -> float * {
+                const int j = w.sk_tile - int(sk_start(p, v) / p.num_kb);
+                return p.sk_ws + ((int64_t(2 * v + j) * kRanks + int64_t(rank)) * p.sk_rows + r) * p.bn + col;
+            };
+            // One pass over this warp's chunks.  mode 0: plain epilogue; 1: store
+            // this CTA's piece; 2: add the tile's pieces, then the plain epilogue.
+            auto chunks = [&](int mode) {
+                int idx = 0;
+                for (int h = 0; h < p.m_halves; ++h) {
+                    // this warp's accumulator rows: quarter_rows of them, from TMEM lane 32q;
+                    // with 16 rows (M = 64) lanes 16-31 load and stage values the store leaves out
+                    const int row0 = m0 + h * 128 + q * p.quarter_rows;
+                    if (row0 >= p.M) continue;  // warp-uniform
+                    const int prow = h * 128 + q * p.quarter_rows + lane;  // row within this CTA's part
+                    for (int c = 0; c * kEpiCols < p.bn; ++c) {
+                        const int col0 = n0 + c * kEpiCols;
+                        if (col0 >= p.N) break;  // warp-uniform
+                        if ((idx++ & 1) != sub) continue;  // the other warp of this quarter takes it
+                        // the chunk's TMEM columns, staging buffer and store box lie inside their regions,
+                        // a piece's row and columns inside its workspace slot
+                        if (!check(a * p.acc_cols + h * p.bn + (c + 1) * kEpiCols <= p.tmem_cols &&
+                                       uint32_t((warp - 1) * nbuf) * p.c_buf_bytes <= p.off_bar - p.off_c &&
+                                       col0 % 8 == 0 && w.row_off + row0 >= 0 &&
+                                       (mode == 0 || (h * 128 + (q + 1) * p.quarter_rows <= p.sk_rows &&
+                                                      w.sk_tile < p.sk_tiles && lo >= 0 && hi < p.workers)),
+                                   p, abort, 2, tiles_done))
+                            continue;
+                        uint32_t v[32];
+                        if (p.num_kb > 0) {
+                            tmem_ld_32x32b_x32(tmem + lane_base + uint32_t(a * p.acc_cols + h * p.bn + c * kEpiCols),
+                                               v);
+                            tmem_wait_ld();
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0u;  // empty reduction
-                    }
-                    const uint32_t buf = my_bufs + (nbuf == 2 ? (chunk & 1u) : 0u) * p.c_buf_bytes;
-                    if (chunk >= uint32_t(nbuf) && lane == 0) {  // buffer's previous store has read it
-                        if (nbuf == 2)
-                            bulk_wait_read<1>();
-                        else
-                            bulk_wait_read<0>();
-                    }
-                    __syncwarp();
-                    if (p.out_mode == 0) {
-                        // fp32: 128-byte rows, 128-byte swizzle (16-byte chunk j of row r at j ^ (r % 8))
-                        const uint32_t row = buf + uint32_t(lane) * 128u;
+                            for (int e = 0; e < 32; ++e) v[e] = 0u;  // empty reduction
+                        }
+                        if (mode == 1) {
+                            if (lane < p.quarter_rows) {
+                                float4 *dst = reinterpret_cast<float4 *>(piece_at(unit0, prow, c * kEpiCols));
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            st_shared_v4(row + (uint32_t(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                                         v[4 * j + 3]);
-                    } else {
-                        // 16-bit: 64-byte rows, 64-byte swizzle (chunk j of row r at j ^ ((r / 2) % 4))
-                        const uint32_t row = buf + uint32_t(lane) * 64u;
+                                for (int e = 0; e < 8; ++e)
+                                    dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                            }
+                            continue;
+                        }
+                        if (mode == 2 && lane < p.quarter_rows) {
+                            // the pieces of workers lo .. hi in that (k) order; this CTA's own is v
+                            float4 acc[8];
+                            for (int vw = lo; vw <= hi; ++vw) {
+                                float4 x[8];
+                                if (vw == unit0) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float x0 = __uint_as_float(v[8 * j + 2 * e]);
-                                const float x1 = __uint_as_float(v[8 * j + 2 * e + 1]);
-                                if (p.out_mode == 1) {
-                                    __half2 h2 = __floats2half2_rn(x0, x1);
-                                    w[e] = *reinterpret_cast<uint32_t *>(&h2);
+                                    for (int e = 0; e < 8; ++e)
+                                        x[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                                           __uint_as_float(v[4 * e + 2]),
+                                                           __uint_as_float(v[4 * e + 3]));
                                 } else {
-                                    __nv_bfloat162 b2 = __floats2bfloat162_rn(x0, x1);
-                                    w[e] = *reinterpret_cast<uint32_t *>(&b2);
+                                    const float4 *src =
+                                        reinterpret_cast<const float4 *>(piece_at(vw, prow, c * kEpiCols));
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) x[e] = __ldcg(src + e);
+                                }
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    if (vw == lo) {
+                                        acc[e] = x[e];
+                                    } else {
+                                        acc[e].x += x[e].x;
+                                        acc[e].y += x[e].y;
+                                        acc[e].z += x[e].z;
+                                        acc[e].w += x[e].w;
+                                    }
                                 }
                             }
-                            st_shared_v4(row + (uint32_t(j ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                v[4 * e] = __float_as_uint(acc[e].x);
+                                v[4 * e + 1] = __float_as_uint(acc[e].y);
+                                v[4 * e + 2] = __float_as_uint(acc[e].z);
+                                v[4 * e + 3] = __float_as_uint(acc[e].w);
+                            }
                         }
+                        const uint32_t buf = my_bufs + (nbuf == 2 ? (chunk & 1u) : 0u) * p.c_buf_bytes;
+                        if (chunk >= uint32_t(nbuf) && lane == 0) {  // buffer's previous store has read it
+                            if (nbuf == 2)
+                                bulk_wait_read<1>();
+                            else
+                                bulk_wait_read<0>();
+                        }
+                        __syncwarp();
+                        if (p.out_mode == 0) {
+                            // fp32: 128-byte rows, 128-byte swizzle (16-byte chunk j of row r at j ^ (r % 8))
+                            const uint32_t row = buf + uint32_t(lane) * 128u;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                st_shared_v4(row + (uint32_t(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1],
+                                             v[4 * j + 2], v[4 * j + 3]);
+                        } else {
+                            // 16-bit: 64-byte rows, 64-byte swizzle (chunk j of row r at j ^ ((r / 2) % 4))
+                            const uint32_t row = buf + uint32_t(lane) * 64u;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                uint32_t hw[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float x0 = __uint_as_float(v[8 * j + 2 * e]);
+                                    const float x1 = __uint_as_float(v[8 * j + 2 * e + 1]);
+                                    if (p.out_mode == 1) {
+                                        __half2 h2 = __floats2half2_rn(x0, x1);
+                                        hw[e] = *reinterpret_cast<uint32_t *>(&h2);
+                                    } else {
+                                        __nv_bfloat162 b2 = __floats2bfloat162_rn(x0, x1);
+                                        hw[e] = *reinterpret_cast<uint32_t *>(&b2);
+                                    }
+                                }
+                                st_shared_v4(row + (uint32_t(j ^ ((lane >> 1) & 3)) << 4), hw[0], hw[1], hw[2], hw[3]);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&p.tmC, col0, w.row_off + row0, buf);
+                            bulk_commit();
+                        }
+                        ++chunk;
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&p.tmC, col0, w.row_off + row0, buf);
-                        bulk_commit();
-                    }
-                    ++chunk;
+                }
+            };
+            if (!piece) {
+                chunks(0);
+            } else {
+                chunks(1);
+                __threadfence();  // this thread's piece is visible GPU-wide before the count below
+                sk_ok = epi_sync();
+                if (sk_ok && threadIdx.x == 2 * 32) {
+                    int *cnt = p.sk_cnt + w.sk_tile * kRanks + int(rank);
+                    const int last = atomicAdd(cnt, 1) == hi - lo;
+                    if (last) *cnt = 0;  // every piece of this launch is in: ready for the next launch
+                    *flag = last;
+                }
+                sk_ok = sk_ok && epi_sync();
+                if (sk_ok && *reinterpret_cast<volatile int *>(flag)) {
+                    __threadfence();
+                    chunks(2);
                 }
             }
             // All TMEM reads of accumulator a are done: hand it back to the MMA warp.
@@ -923,10 +1081,11 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                 a = 0;
                 aph ^= 1u;
             }
+            if (!sk_ok) break;  // the epilogue warps lost step: give up (the timeout is recorded)
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
-        if (p.grid_reduce) grid_reduce_phase(p, abort, reinterpret_cast<int *>(smem + p.off_bar - 16));
+        if (p.grid_reduce) grid_reduce_phase(p, abort, flag);
     }
 
     tc_fence_before();
@@ -1060,6 +1219,8 @@ struct tgemm_plan_s {
     int *d_counters;           // csk with more than one cluster per tile: arrival counters
     int grid_reduce;           // K splits reduced in the GEMM kernel after a grid-wide barrier
     uint32_t *d_gbar;          // that barrier's arrival count and generation
+    int sk_tiles;              // tiles of the stream-K tail (0: none)
+    float *d_sk_ws;            // the tail's partial pieces
     int *d_status;
     unsigned long long watchdog_ns;
     int debug_stall;
@@ -1096,7 +1257,7 @@ static int allow_max_smem(int dev, int limit)
 // splits; prefetch: the producer's lead in k-blocks.
 static void fill_params(Params &q, const Layout &L, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
                         int block_M, int block_N, int block_K, int num_stages, int pair, int splits, int prefetch,
-                        int group_m, int tiles_m, int tiles_n, int csk = 0)
+                        int group_m, int tiles_m, int tiles_n, int workers, int csk = 0)
 {
     std::memset(&q, 0, sizeof(q));
     q.M = int(M);
@@ -1134,6 +1295,12 @@ static void fill_params(Params &q, const Layout &L, int64_t M, int64_t N, int64_
     // The kernel's own output: fp32 partials when K is split and reduced by a
     // second kernel, else C's type.
     q.out_mode = splits > 1 && csk <= 1 ? 0 : out_dtype == kF32 ? 0 : out_dtype == kF16 ? 1 : 2;
+    // Persistent schedule: workers take whole units round robin; a plan with a
+    // stream-K tail sets dp_units and sk_tiles afterwards.
+    q.workers = workers;
+    q.dp_units = q.num_units;
+    q.sk_tiles = 0;
+    q.sk_rows = L.m_halves * 4 * L.quarter_rows;
     q.csk = csk > 1 ? csk : 0;
     q.outer = csk > 1 ? splits / csk : 1;
     q.slice_w = csk > 1 ? block_N / csk : 0;
@@ -1211,6 +1378,8 @@ static int check_opts(const tgemm_plan_opts *opts, int num_stages)
         return kErrInvalidArg;
     if (opts->stream_operands != 0 && opts->stream_operands != 1) return kErrInvalidArg;
     if (opts->grid_reduce != 0 && opts->grid_reduce != 1) return kErrInvalidArg;
+    if (opts->stream_k != 0 && opts->stream_k != 1) return kErrInvalidArg;
+    if (opts->stream_k && (opts->split_k > 1 || opts->cluster_k > 1)) return kErrInvalidArg;
     return kOk;
 }
 
@@ -1321,6 +1490,8 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     p->d_counters = nullptr;
     p->grid_reduce = splits > 1 && !csk && opts && opts->grid_reduce ? 1 : 0;
     p->d_gbar = nullptr;
+    p->sk_tiles = 0;
+    p->d_sk_ws = nullptr;
     p->device = dev;
     p->num_sms = sms;
     p->smem_limit = limit;
@@ -1397,6 +1568,14 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
         }
         p->grid = units;
     }
+    if (opts && opts->stream_k) {
+        // Stream-K tail: the tiles past the last whole wave of workers, shared out
+        // as runs of k-blocks, if each worker gets at least two of them.
+        const int workers = pair ? p->grid / 2 : p->grid;
+        const int kb = int((K + block_K - 1) / block_K);
+        const int rem = p->num_tiles % workers;
+        if (rem > 0 && int64_t(rem) * kb >= 2 * int64_t(workers)) p->sk_tiles = rem;
+    }
     const int outer = csk ? splits / csk : splits;  // partial sums that go through the workspace
     if (splits > 1 && outer > 1) {
         const size_t bytes = size_t(outer) * size_t(p->tiles_m) * size_t(block_M) * size_t(N) * sizeof(float);
@@ -1418,6 +1597,23 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
             return kErrCuda;
         }
     }
+    if (p->sk_tiles) {
+        const int workers = pair ? p->grid / 2 : p->grid;
+        const size_t rows = size_t(p->L.m_halves) * 4 * size_t(p->L.quarter_rows);
+        const size_t ws = size_t(workers) * 2 * (pair ? 2 : 1) * rows * size_t(block_N) * sizeof(float);
+        const size_t cnt = size_t(p->sk_tiles) * (pair ? 2 : 1) * sizeof(int);
+        if (cudaMalloc(&p->d_sk_ws, ws) != cudaSuccess || cudaMalloc(&p->d_counters, cnt) != cudaSuccess ||
+            cudaMemset(p->d_counters, 0, cnt) != cudaSuccess) {
+            cudaGetLastError();
+            if (p->d_counters) cudaFree(p->d_counters);
+            if (p->d_sk_ws) cudaFree(p->d_sk_ws);
+            if (p->d_gbar) cudaFree(p->d_gbar);
+            if (p->d_work) cudaFree(p->d_work);
+            cudaFree(p->d_status);
+            delete p;
+            return kErrCuda;
+        }
+    }
     if (csk && outer > 1) {
         const size_t bytes = size_t(p->num_tiles) * size_t(csk) * sizeof(int);
         if (cudaMalloc(&p->d_counters, bytes) != cudaSuccess || cudaMemset(p->d_counters, 0, bytes) != cudaSuccess) {
@@ -1432,11 +1628,16 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
 
     Params &q = p->params;
     fill_params(q, p->L, M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, pair, splits,
-                opts && opts->prefetch > 0 ? opts->prefetch : num_stages, p->group_m, p->tiles_m, p->tiles_n, csk);
+                opts && opts->prefetch > 0 ? opts->prefetch : num_stages, p->group_m, p->tiles_m, p->tiles_n,
+                pair ? p->grid / 2 : p->grid, csk);
     q.watchdog_ns = p->watchdog_ns;
     q.status = p->d_status;
     q.ws = p->d_work;
     q.counters = p->d_counters;
+    q.dp_units = q.num_units - p->sk_tiles;
+    q.sk_tiles = p->sk_tiles;
+    q.sk_ws = p->d_sk_ws;
+    q.sk_cnt = p->d_counters;
     q.stream_ops = opts && opts->stream_operands ? 1 : 0;
     q.grid_reduce = p->grid_reduce;
     q.grid_bar = p->d_gbar;
@@ -1558,9 +1759,8 @@ int tgemm_status(tgemm_plan_t p, int *detail)
     }
     // A launch that gave up may have left some of the in-kernel split
     // reduction's arrival counters part-way: clear them for the next launch.
-    if (h[0] != kOk && ((p->d_counters &&
-                         cudaMemset(p->d_counters, 0, size_t(p->num_tiles) * size_t(p->csk) * sizeof(int)) !=
-                             cudaSuccess) ||
+    const size_t n_counters = p->sk_tiles ? size_t(p->sk_tiles) * (p->pair ? 2 : 1) : size_t(p->num_tiles) * p->csk;
+    if (h[0] != kOk && ((p->d_counters && cudaMemset(p->d_counters, 0, n_counters * sizeof(int)) != cudaSuccess) ||
                         (p->d_gbar && cudaMemset(p->d_gbar, 0, 2 * sizeof(uint32_t)) != cudaSuccess))) {
         cudaGetLastError();
         return -kErrCuda;
@@ -1614,6 +1814,7 @@ int tgemm_get_plan_info(tgemm_plan_t p, tgemm_plan_info *info)
     info->cluster_k = p->csk;
     info->stream_operands = p->params.stream_ops;
     info->grid_reduce = p->grid_reduce;
+    info->stream_k_tiles = p->sk_tiles;
     return kOk;
 }
 
@@ -1634,6 +1835,10 @@ int tgemm_destroy(tgemm_plan_t p)
         rc = kErrCuda;
     }
     if (p->d_gbar && cudaFree(p->d_gbar) != cudaSuccess) {
+        cudaGetLastError();
+        rc = kErrCuda;
+    }
+    if (p->d_sk_ws && cudaFree(p->d_sk_ws) != cudaSuccess) {
         cudaGetLastError();
         rc = kErrCuda;
     }
@@ -1746,7 +1951,7 @@ extern "C" int tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype, int
 
     Params q;
     fill_params(q, L, M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, 0, 1, num_stages, 8,
-                tiles_m, tiles_n);
+                tiles_m, tiles_n, grid);
     q.watchdog_ns = env_watchdog();
     q.status = scratch;
     rc = encode_maps(q, L, dtype, out_dtype, A, B, C, nullptr);

@@ -36,7 +36,8 @@ FROZEN = {
     (128, 128, 128, 0, 2): dict(block=(128, 128, 32), num_stages=3),
 }
 
-DEFAULT_OPTS = dict(cta_pair=False, split_k=1, group_m=0, cluster_k=0, stream_operands=False, grid_reduce=False)
+DEFAULT_OPTS = dict(cta_pair=False, split_k=1, group_m=0, cluster_k=0, stream_operands=False, grid_reduce=False,
+                    stream_k=False)
 
 # Candidate tiles: (block, depth, relative steady-state throughput per SM
 # measured at full waves on GB300 with one CTA 256x256 = 1, CTA pair).  A

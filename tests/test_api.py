@@ -48,7 +48,7 @@ C_PROGRAM = r"""
 
 int main(void)
 {
-    tgemm_plan_opts opts = {1, 2, 1, 0, 0, 0, 0};  /* cta_pair, group_m, split_k, prefetch, cluster_k, stream, grid_reduce */
+    tgemm_plan_opts opts = {1, 2, 1, 0, 0, 0, 0, 0};  /* pair, group, split, prefetch, cluster, stream, grid, stream-K */
     int64_t bound = tgemm_smem_bound(TGEMM_F16, 128, 128, 32, 3);
     int one = tgemm_validate(4096, 4096, 4096, TGEMM_F16, TGEMM_F16, 256, 224, 64, 3, 232448);
     int pair = tgemm_validate_ex(4096, 4096, 4096, TGEMM_F16, TGEMM_F16, 256, 224, 128, 3, 232448, &opts);
@@ -199,6 +199,55 @@ def test_validate_ex_stream_operands_and_grid_reduce(lib):
     for v, want in ((0, tg.OK), (1, tg.OK), (2, tg.ERR_INVALID_ARG), (-1, tg.ERR_INVALID_ARG)):
         assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, LIMIT_227K, stream_operands=v) == want
         assert V(512, 512, 512, tg.F16, tg.F32, 128, 128, 64, 4, LIMIT_227K, split_k=4, grid_reduce=v) == want
+
+
+def test_validate_ex_stream_k_rules(lib):
+    V = tg.tgemm_validate_ex
+    L = LIMIT_227K
+    assert V(4000, 3000, 5000, tg.F16, tg.F32, 256, 352, 64, 5, L, cta_pair=1, stream_k=1) == tg.OK
+    assert V(4000, 3000, 5000, tg.F16, tg.F32, 256, 352, 64, 5, L, cta_pair=1, stream_k=2) == tg.ERR_INVALID_ARG
+    # the tail is shared by k-blocks: not combined with a K split or the cluster reduction
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 4, L, split_k=2, stream_k=1) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 4, L, split_k=8, cluster_k=4,
+             stream_k=1) == tg.ERR_INVALID_ARG
+
+
+def stream_k_tail(T, G, KB):
+    """The stream-K tail as the header states it: tiles past the last whole
+    wave of G workers, if each worker gets at least two of their k-blocks;
+    worker w takes iterations [I*w/G, I*(w+1)/G) of the I = R*KB total."""
+    R = T % G
+    if R == 0 or R * KB < 2 * G:
+        return None
+    I = R * KB
+    return [(I * w // G, I * (w + 1) // G) for w in range(G)]
+
+
+def test_stream_k_tail_partition_by_brute_force():
+    # Every tail tile is covered exactly once, in k order, by consecutive
+    # workers; no worker touches more than two tail tiles; the kernel's closed
+    # forms for a tile's first and last worker (ceil(G*(t*KB+1)/I) - 1 and
+    # ceil(G*(t+1)*KB/I) - 1) agree with a search.
+    for G in (1, 3, 76, 152):
+        for T in range(1, 330, 7):
+            for KB in (1, 2, 5, 33, 79, 128):
+                ranges = stream_k_tail(T, G, KB)
+                if ranges is None:
+                    continue
+                R, I = T % G, (T % G) * KB
+                owners = {}
+                for w, (s0, s1) in enumerate(ranges):
+                    if s0 < s1:
+                        assert (s1 - 1) // KB - s0 // KB <= 1
+                    for k in range(s0, s1):
+                        owners.setdefault(k // KB, []).append((w, k % KB))
+                for t in range(R):
+                    ks = [k for _, k in owners[t]]
+                    assert ks == list(range(KB))
+                    ws = [w for w, _ in owners[t]]
+                    assert ws == sorted(ws)
+                    assert -(-(G * (t * KB + 1)) // I) - 1 == ws[0]
+                    assert -(-(G * (t + 1) * KB) // I) - 1 == ws[-1]
 
 
 def test_validate_ex_cluster_k_rules(lib):

@@ -553,3 +553,74 @@ def test_gemm_from_several_host_threads(cuda_lib):
         for C in outs:
             assert torch.equal(C, outs[0])
         assert_close(as_f64(outs[0]), R, S, "f32")
+
+
+# ------------------------------------------------------------ stream-K tail of the persistent schedule
+
+SK_CASES = [
+    # (shape, block, stages, pair): tiles past the last whole wave of workers are
+    # shared out by k-blocks (the persistent grid has one worker per SM or pair)
+    ((4000, 3000, 5000), (256, 352, 64), 5, True),    # the ragged default: 144 tiles on 76 pairs
+    ((3000, 2080, 1032), (256, 256, 128), 3, True),   # 108 tiles: 32 past one wave of pairs
+    ((2304, 2304, 4096), (256, 256, 64), 3, True),    # 81 tiles: 5 past the wave, each in ~15 pieces
+    ((2000, 2080, 1032), (128, 128, 64), 4, False),   # 272 tiles on 152 CTAs
+    ((3000, 2080, 1032), (256, 128, 64), 3, False),   # one CTA, two M-halves per tile
+    ((2000, 1304, 2048), (64, 256, 64), 4, False),    # 64-row tiles
+]
+
+
+@pytest.mark.parametrize("shape,block,stages,pair", SK_CASES, ids=lambda v: str(v))
+@pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("bf16", "bf16")])
+def test_stream_k_parity(cuda_lib, shape, block, stages, pair, dtype, out):
+    M, N, K = shape
+    A, B = inputs.operands(800 + M % 97, M, N, K, dtype, "uniform")
+    plan = cuda_lib.Plan(M, N, K, dtype, out, block, stages, pair=pair, stream_k=True)
+    assert plan.info["stream_k_tiles"] > 0
+    plan.close()
+    C = as_f64(run_sk(cuda_lib, A, B, dtype, out, block, stages, pair))
+    R, S = oracle.gemm(A, B, dtype)
+    assert_close(C, R, S, out)
+
+
+def run_sk(tg, A, B, dtype, out, block, stages, pair):
+    M, K = A.shape
+    N = B.shape[0]
+    plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair, stream_k=True)
+    C = torch.full((M, N), float("nan"), dtype=TORCH[out], device="cuda")
+    plan.run(to_dev(A, dtype), to_dev(B, dtype), C)
+    torch.cuda.synchronize()
+    rc, detail = plan.status()
+    assert rc == 0, f"kernel status {rc} {detail}"
+    plan.close()
+    return C
+
+
+@pytest.mark.parametrize("shape,block,stages,pair", SK_CASES, ids=lambda v: str(v))
+def test_stream_k_integer_exact_repeatable_and_stage_invariant(cuda_lib, shape, block, stages, pair):
+    M, N, K = shape
+    A, B = inputs.operands(43, M, N, K, "f16", "int", lo=-4, hi=4)
+    dA, dB = to_dev(A, "f16"), to_dev(B, "f16")
+    outs = []
+    for s in sorted({1, 2, stages}):
+        plan = cuda_lib.Plan(M, N, K, "f16", "f32", block, s, pair=pair, stream_k=True)
+        for _ in range(2):  # the tail's counters reset themselves between launches
+            outs.append(plan.run(dA, dB))
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+        plan.close()
+    R, _ = oracle.gemm(A, B, "f16")
+    assert np.array_equal(as_f64(outs[0]), R)
+    for C in outs[1:]:
+        assert torch.equal(C, outs[0])
+    # random values: the pieces are added in a fixed order, so the bits repeat too
+    A, B = inputs.operands(44, M, N, K, "bf16", "normal")
+    dA, dB = to_dev(A, "bf16"), to_dev(B, "bf16")
+    outs = []
+    for s in sorted({2, stages}):
+        plan = cuda_lib.Plan(M, N, K, "bf16", "f32", block, s, pair=pair, stream_k=True)
+        outs += [plan.run(dA, dB), plan.run(dA, dB)]
+        torch.cuda.synchronize()
+        assert plan.status()[0] == 0
+        plan.close()
+    for C in outs[1:]:
+        assert torch.equal(C.view(torch.int32), outs[0].view(torch.int32))

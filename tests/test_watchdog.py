@@ -20,17 +20,20 @@ pytestmark = pytest.mark.gpu
     ((128, 128, 32), 3, False, 1, 0), ((128, 256, 64), 1, False, 1, 0), ((256, 256, 64), 4, True, 1, 0),
     ((128, 256, 64), 4, False, 8, 4),  # K splits reduced in the kernel by clusters of 4: both cluster levels
     ((256, 256, 64), 3, True, 4, -1),  # K splits reduced in the kernel after a grid-wide barrier
+    ((64, 64, 32), 4, False, 1, -2),   # a stream-K tail (1024 x 1024: 256 tiles on 152 CTAs)
 ])
 def test_stall_reports_timeout_and_context_survives(cuda_lib, block, stages, pair, split_k, cluster_k):
-    grid_reduce = cluster_k == -1
+    grid_reduce, stream_k = cluster_k == -1, cluster_k == -2
     cluster_k = max(cluster_k, 0)
-    M, N, K = 512, 512, 512
+    M, N, K = (1024, 1024, 512) if stream_k else (512, 512, 512)
     A, B = inputs.operands(31, M, N, K, "f16", "uniform")
     dA = inputs.bits_to_torch(A, "f16").cuda()
     dB = inputs.bits_to_torch(B, "f16").cuda()
     C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
     plan = cuda_lib.Plan(M, N, K, "f16", "f32", block, stages, pair=pair, split_k=split_k, cluster_k=cluster_k,
-                         grid_reduce=grid_reduce)
+                         grid_reduce=grid_reduce, stream_k=stream_k)
+    if stream_k:
+        assert plan.info["stream_k_tiles"] > 0
     plan.set_watchdog_ns(50_000_000)
     plan.debug_stall(True)
     plan.run(dA, dB, C)
