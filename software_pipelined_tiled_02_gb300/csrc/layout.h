@@ -152,7 +152,7 @@ inline bool csplit_supported(int bm, int bn, int pair, int eff_splits, int csk)
     if (csk != 2 && csk != 4 && csk != 8) return false;
     if (pair || bm != 128) return false;
     if (eff_splits % csk != 0) return false;
-    return bn % csk == 0 && (bn / csk) % kEpiCols == 0;
+    return bn % csk == 0 && (bn / csk) % kEpiCols == 0 && bn / csk <= 128;
 }
 
 inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int bm, int bn, int bk,

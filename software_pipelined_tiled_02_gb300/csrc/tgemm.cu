@@ -514,8 +514,9 @@ __device__ __noinline__ void grid_reduce_phase(const Params &p, volatile int *ab
 // global stores are contiguous), read eight different bank groups.
 
 // Items (16-byte column groups of one slice row) per epilogue thread:
-// 128 x slice_w / 4 over 256 threads = slice_w / 8, so 4, 8 or 16; a slice row
-// has 2 x NIT column groups.
+// 128 x slice_w / 4 over 256 threads = slice_w / 8 -- 4, 8, 12 or 16 for the
+// slices of 32, 64, 96 and 128 columns that block_N <= 256 and csk >= 2
+// allow; a slice row has 2 x NIT column groups.
 template <int NIT>
 __device__ __forceinline__ void csplit_finish(const Params &p, uint32_t sA, int *flag, int tile, int o,
                                               uint32_t crank, int grow0, int gcol0, uint32_t part_bytes)
@@ -663,7 +664,9 @@ __device__ __noinline__ void csplit_epilogue(const Params &p, uint32_t sA, int *
     switch (p.slice_w) {
     case 32: csplit_finish<4>(p, sA, flag, tile, o, crank, grow0, gcol0, part_bytes); break;
     case 64: csplit_finish<8>(p, sA, flag, tile, o, crank, grow0, gcol0, part_bytes); break;
-    default: csplit_finish<16>(p, sA, flag, tile, o, crank, grow0, gcol0, part_bytes); break;
+    case 96: csplit_finish<12>(p, sA, flag, tile, o, crank, grow0, gcol0, part_bytes); break;
+    case 128: csplit_finish<16>(p, sA, flag, tile, o, crank, grow0, gcol0, part_bytes); break;
+    default: check(false, p, abort, 2, p.slice_w); break;  // the plan admits no other slice width
     }
 }
 

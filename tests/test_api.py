@@ -271,6 +271,8 @@ def test_validate_ex_cluster_k_rules(lib):
     # slices of block_N / cluster_k columns must be whole 32-column chunks
     assert V(512, 512, 32768, tg.F16, tg.F32, 128, 128, 64, 4, L, split_k=16, cluster_k=8) == tg.ERR_INVALID_ARG
     assert V(512, 512, 32768, tg.F16, tg.F32, 128, 96, 64, 4, L, split_k=16, cluster_k=2) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 224, 64, 4, L, split_k=16, cluster_k=2) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 32768, tg.F16, tg.F32, 128, 192, 64, 4, L, split_k=16, cluster_k=2) == tg.OK  # 96
     # the exchanged partials (128 x block_N x 4 bytes) must fit the operand ring
     assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 2, L, **ok) == tg.ERR_SMEM_BUDGET  # 96 KB < 128 KB
     assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 3, L, **ok) == tg.OK              # 144 KB

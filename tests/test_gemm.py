@@ -408,6 +408,8 @@ CSPLIT_CONFIGS = [
     ((128, 128, 64), 4, 8, 4),
     ((128, 64, 32), 5, 2, 2),
     ((128, 256, 32), 6, 24, 8),
+    ((128, 192, 64), 4, 4, 2),     # 96-column slices
+    ((128, 192, 32), 6, 6, 2),
 ]
 
 
