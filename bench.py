@@ -505,7 +505,9 @@ def run_ours(args, w, world, rank, local):
     algo_bytes = (M * K + N * K) * 2 + M * N * (4 if w["out"] == "f32" else 2)
     two_kernels = info["split_k"] > 1 and info["cluster_k"] <= 1 and not info["grid_reduce"]
     roofline = roofline_for(flops, algo_bytes, mean_ms / 1e3, measured_peaks())
-    roofline.update({"traffic": recorded_traffic(args.workload,
+    roofline.update({"traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, L2 clean "
+                                     "at its start; output still in L2 when the launch ends is not counted",
+                     "traffic": recorded_traffic(args.workload,
                                                  config_key(block, stages, pair, info["split_k"], group_m,
                                                             info["cluster_k"], info["stream_operands"],
                                                             info["grid_reduce"])),
