@@ -79,11 +79,12 @@ inline bool tile_supported(int bm, int bn, int bk, int in_bytes, int pair = 0)
 }
 
 // Barrier block: full[S], empty[S], acc_full[2], acc_empty[2], drain, stall,
-// epi (the epilogue warps' own barrier) (8 bytes each), then the TMEM base
-// address word, the abort flag, and a word through which one epilogue thread
-// tells the others whether its CTA counted in last (stream-K and in-kernel
-// split reductions), plus padding.
-inline uint32_t barrier_block_bytes(int stages) { return round_up((2u * stages + 7u) * 8u + 16u, 16u); }
+// epi (the epilogue warps' own barrier), bulk (the in-kernel split
+// reduction's copies) (8 bytes each), then the TMEM base address word, the
+// abort flag, and a word through which one epilogue thread tells the others
+// whether its CTA counted in last (stream-K and in-kernel split reductions),
+// plus padding.
+inline uint32_t barrier_block_bytes(int stages) { return round_up((2u * stages + 8u) * 8u + 16u, 16u); }
 
 inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out_dtype, int pair = 0)
 {

@@ -99,6 +99,16 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// Untiled bulk copy of `bytes` contiguous bytes (a multiple of 16; both
+// addresses 16-byte aligned) from global to this CTA's shared memory,
+// completing `bar`'s transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // 2-D tiled store of a shared-memory box to (x, y); out-of-range elements of
 // the box are not written.
 __device__ __forceinline__ void tma_store_2d(const void *tmap, int32_t x, int32_t y, uint32_t src)

@@ -405,7 +405,8 @@ __device__ __forceinline__ void mma_dispatch_nk(const Params &p, const MmaCtx &c
 // separate reduction kernel, so both give the same bits -- and round once to
 // C's type.  The barrier resets itself (arrivals back to 0), so launches need
 // no host-side state; its wait is bounded by the watchdog.
-__device__ __noinline__ void grid_reduce_phase(const Params &p, volatile int *abort, int *flag)
+__device__ __noinline__ void grid_reduce_phase(const Params &p, volatile int *abort, int *flag, uint32_t sA,
+                                               uint32_t bulk_bar)
 {
     const int et = int(threadIdx.x) - 2 * 32;  // 0..255 over the eight epilogue warps
     if ((threadIdx.x & 31u) == 0) {
@@ -437,49 +438,62 @@ __device__ __noinline__ void grid_reduce_phase(const Params &p, volatile int *ab
     named_bar_sync(1, 8 * 32);
     if (!*reinterpret_cast<volatile int *>(flag)) return;
     __threadfence();
-    // Partial of split s at element e: ws[s * split_rows * N + e] (e < M * N;
-    // M * N and the split stride are multiples of 4).  A thread issues the
-    // loads of up to CH splits of its element, predicated rather than
-    // branched, before adding any of them.
-    constexpr int CH = 24;
+    // CTA b reduces a contiguous run of the M x N outputs, in 16-byte groups:
+    // [b * per, (b + 1) * per).  Split s's partial of output e sits at
+    // ws[s * split_rows * N + e].  One thread copies the run of every split
+    // into this CTA's operand ring (idle now: all its MMAs are done) with
+    // bulk copies on one mbarrier; then the epilogue threads add the splits
+    // in order 0, 1, ..., splits-1 from shared memory and round once to C's
+    // type.  Runs longer than the ring allows are done in rounds.
     const int64_t n4 = int64_t(p.M) * p.N / 4;
+    const int64_t per = (n4 + gridDim.x - 1) / gridDim.x;
+    const int64_t b0 = int64_t(blockIdx.x) * per;
+    const int64_t b1 = b0 + per < n4 ? b0 + per : n4;
     const int64_t stride4 = int64_t(p.split_rows) * p.N / 4;
     const float4 *W = reinterpret_cast<const float4 *>(p.ws);
-    for (int64_t i = int64_t(blockIdx.x) * 256 + et; i < n4; i += int64_t(gridDim.x) * 256) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < p.splits; s0 += CH) {
-            float4 v[CH];
-#pragma unroll
-            for (int t = 0; t < CH; ++t)
-                if (s0 + t < p.splits) v[t] = __ldcg(W + int64_t(s0 + t) * stride4 + i);
-#pragma unroll
-            for (int t = 0; t < CH; ++t) {
-                if (s0 + t < p.splits) {
-                    if (s0 + t == 0) {
-                        acc = v[t];
-                    } else {
-                        acc.x += v[t].x;
-                        acc.y += v[t].y;
-                        acc.z += v[t].z;
-                        acc.w += v[t].w;
-                    }
-                }
-            }
+    const int64_t chunk = int64_t(p.off_c - p.off_a) / 16 / p.splits;  // 16-byte groups per split per round
+    uint32_t ph = 0;
+    for (int64_t c0 = b0; c0 < b1; c0 += chunk) {
+        const int64_t cnt = b1 - c0 < chunk ? b1 - c0 : chunk;
+        named_bar_sync(1, 8 * 32);  // the previous round's reads of the ring are done
+        if (et == 0) {
+            fence_proxy_async_global();  // the partials, read through the async proxy below
+            mbar_arrive_expect_tx(bulk_bar, uint32_t(cnt * 16 * p.splits));
+            for (int s = 0; s < p.splits; ++s)
+                bulk_load(sA + uint32_t(s * chunk * 16), W + int64_t(s) * stride4 + c0, uint32_t(cnt * 16), bulk_bar);
         }
-        if (p.out_mode_final == 0) {
-            reinterpret_cast<float4 *>(p.C)[i] = acc;
-        } else if (p.out_mode_final == 1) {
-            __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
-            uint2 u;
-            u.x = *reinterpret_cast<uint32_t *>(&lo);
-            u.y = *reinterpret_cast<uint32_t *>(&hi);
-            reinterpret_cast<uint2 *>(p.C)[i] = u;
-        } else {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-            uint2 u;
-            u.x = *reinterpret_cast<uint32_t *>(&lo);
-            u.y = *reinterpret_cast<uint32_t *>(&hi);
-            reinterpret_cast<uint2 *>(p.C)[i] = u;
+        // Every epilogue warp waits for the copies (bounded: on expiry the wait
+        // records the timeout and raises the abort flag), then all meet, so that
+        // they read the flag alike and leave together.
+        warp_wait(bulk_bar, ph, p, abort, 2, -2, false);
+        ph ^= 1u;
+        named_bar_sync(1, 8 * 32);
+        if (*abort) return;
+        for (int64_t i = et; i < cnt; i += 8 * 32) {
+            float4 acc = ld_shared_v4f(sA + uint32_t(i * 16));
+            for (int s = 1; s < p.splits; ++s) {
+                const float4 t = ld_shared_v4f(sA + uint32_t((s * chunk + i) * 16));
+                acc.x += t.x;
+                acc.y += t.y;
+                acc.z += t.z;
+                acc.w += t.w;
+            }
+            const int64_t e = c0 + i;
+            if (p.out_mode_final == 0) {
+                reinterpret_cast<float4 *>(p.C)[e] = acc;
+            } else if (p.out_mode_final == 1) {
+                __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
+                uint2 u;
+                u.x = *reinterpret_cast<uint32_t *>(&lo);
+                u.y = *reinterpret_cast<uint32_t *>(&hi);
+                reinterpret_cast<uint2 *>(p.C)[e] = u;
+            } else {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+                uint2 u;
+                u.x = *reinterpret_cast<uint32_t *>(&lo);
+                u.y = *reinterpret_cast<uint32_t *>(&hi);
+                reinterpret_cast<uint2 *>(p.C)[e] = u;
+            }
         }
     }
 }
@@ -705,8 +719,9 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
     auto acc_empty = [&](int a) { return bars + 8u * uint32_t(2 * S + 2 + a); };
     const uint32_t drain = bars + 8u * uint32_t(2 * S + 4);
     const uint32_t stall = bars + 8u * uint32_t(2 * S + 5);
-    const uint32_t epi_bar = bars + 8u * uint32_t(2 * S + 6);  // the eight epilogue warps meet here
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bar + 8u * uint32_t(2 * S + 7));
+    const uint32_t epi_bar = bars + 8u * uint32_t(2 * S + 6);   // the eight epilogue warps meet here
+    const uint32_t bulk_bar = bars + 8u * uint32_t(2 * S + 7);  // the in-kernel split reduction's copies
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bar + 8u * uint32_t(2 * S + 8));
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *flag = reinterpret_cast<int *>(tmem_slot + 2);  // "counted in last", for the epilogue warps
 
@@ -728,6 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         mbar_init(drain, 1);
         mbar_init(stall, 1);
         mbar_init(epi_bar, kEpiWarps);
+        mbar_init(bulk_bar, 1);
         *abort = 0;
         fence_mbar_init();
         if (p.num_kb > 0) {
@@ -1088,7 +1104,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
-        if (p.grid_reduce) grid_reduce_phase(p, abort, flag);
+        if (p.grid_reduce) grid_reduce_phase(p, abort, flag, sA, bulk_bar);
     }
 
     tc_fence_before();
