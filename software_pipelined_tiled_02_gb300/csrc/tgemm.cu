@@ -33,6 +33,15 @@
 // tile depends only on the tile shape (k-block by k-block, 16 at a time), never
 // on num_stages or the schedule, so results are bit-identical across depths.
 //
+// Launch shapes (tgemm_kernel<MODE>): one CTA per tile, or CTA pairs
+// (cta_group::2, M = 256 over two SMs), persistent over work units; or one CTA
+// per (tile, K split) in thread-block clusters that reduce their splits
+// through distributed shared memory.  Split K is otherwise reduced by a
+// second kernel or, after a grid-wide barrier, by this one.  The persistent
+// schedule can also share the tiles of a partial last wave out by k-blocks
+// (a stream-K tail).  Every such combination adds partial sums in an order
+// fixed by the shape and the options alone.
+//
 // Every mbarrier wait is bounded by a %globaltimer watchdog: on expiry the
 // kernel records TGEMM_ERR_TIMEOUT in the plan's status word, stops issuing
 // work, waits (bounded) for its copies and MMAs in flight, frees its tensor
