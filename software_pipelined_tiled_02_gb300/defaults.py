@@ -39,22 +39,26 @@ FROZEN = {
 DEFAULT_OPTS = dict(cta_pair=False, split_k=1, group_m=0, cluster_k=0, stream_operands=False, grid_reduce=False,
                     stream_k=False)
 
-# Candidate tiles: (block, depth, relative steady-state throughput per SM
-# measured at full waves on GB300 with one CTA 256x256 = 1, CTA pair).  A
-# pair computes one 256-row tile on two SMs.
+# Candidate tiles: (block, depth, relative steady-state throughput per SM,
+# CTA pair), measured on GB300 at whole waves.  A pair computes one 256-row
+# tile on two SMs.  The throughputs follow the operand bytes each SM takes in
+# per cycle at the full tensor rate (69 B for pair 256x224, 64 for 256x256, 48
+# for 256x512): 4096^3 at 256x224 reaches 0.87 of peak, 8192^3 at 256x256
+# 0.97-0.99, 6144^3 at 256x512 1727 against 1706 TFLOP/s for 256x256, and
+# 1024x8192x4096 at 256x448 1397 against 1198 for 256x224x64.  Wide tiles keep
+# one accumulator (no epilogue overlap), which their throughput includes.
 CANDIDATES = (
-    ((256, 256, 128), 3, 1.04, True),
-    ((256, 384, 64), 4, 1.04, True),   # two N = 192 MMAs per k-step; measured on 4000x3000x5000
-    ((256, 352, 64), 5, 1.04, True),   # two N = 176 MMAs per k-step
-    ((256, 224, 64), 5, 1.00, True),
-    ((256, 256, 64), 3, 1.00, False),
-    ((256, 224, 64), 3, 0.98, False),
-    ((256, 192, 64), 3, 0.90, False),
-    ((128, 256, 64), 4, 0.90, False),
-    ((128, 224, 64), 4, 0.86, False),
-    ((256, 128, 64), 4, 0.80, False),
-    ((128, 128, 64), 4, 0.60, False),
-    ((128, 64, 64), 4, 0.35, False),
+    ((256, 256, 128), 3, 0.99, True),
+    ((256, 512, 64), 4, 1.00, True),   # two N = 256 MMAs per k-step sharing A
+    ((256, 448, 64), 4, 1.00, True),
+    ((256, 384, 64), 4, 0.98, True),   # measured on 4000x3000x5000
+    ((256, 352, 64), 5, 0.97, True),   # two N = 176 MMAs per k-step
+    ((256, 224, 128), 3, 0.88, True),
+    ((256, 256, 64), 3, 0.95, False),
+    ((256, 224, 64), 3, 0.85, False),
+    ((128, 256, 64), 4, 0.80, False),
+    ((128, 128, 64), 4, 0.55, False),
+    ((128, 64, 64), 4, 0.32, False),
 )
 
 DEFAULT_SMS = 152

@@ -120,3 +120,23 @@ def test_write_and_read_cache(tmp_path, monkeypatch):
     assert len(lat) == 2 and "extra" not in lat[0] and lat[1]["ok"] is False
     monkeypatch.setenv("TGEMM_AUTOTUNE_DISABLE_CACHE", "1")
     assert sweep.load_cached("NVIDIA GB300", "wl") is None
+
+
+def test_estimator_picks_the_measured_best_tiles():
+    # Shapes outside the tuned table: the wave-count estimator chose, on a
+    # GB300, the same tile as a timed search over its candidates.
+    from software_pipelined_tiled_02_gb300 import defaults
+
+    measured_best = {
+        (3072, 3072, 3072): (256, 512, 64),
+        (6144, 6144, 6144): (256, 512, 64),
+        (1024, 8192, 4096): (256, 448, 64),
+        (8192, 1024, 4096): (256, 512, 64),
+        (4096, 4096, 1024): (256, 224, 128),
+        (2048, 2048, 2048): (256, 256, 128),
+    }
+    for (M, N, K), block in measured_best.items():
+        cfg = defaults.choose(M, N, K, tg.F16, tg.F16)
+        assert cfg["block"] == block and cfg["cta_pair"], ((M, N, K), cfg)
+        assert tg.tgemm_validate_ex(M, N, K, tg.F16, tg.F16, *cfg["block"], cfg["num_stages"], 232448,
+                                    cta_pair=1) == tg.OK
