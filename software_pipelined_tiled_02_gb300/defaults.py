@@ -23,8 +23,8 @@ from __future__ import annotations
 FROZEN = {
     # 1643 vs 1607 TFLOP/s for one CTA 256x224x64, group 8
     (4096, 4096, 4096, 0, 0): dict(block=(256, 224, 128), num_stages=3, cta_pair=True, group_m=2),
-    # 1753 vs 1692 for one CTA 256x256x64
-    (8192, 8192, 8192, 1, 1): dict(block=(256, 256, 128), num_stages=3, cta_pair=True),
+    # 1952-1976 vs 1897-1922 for pair 256x256x128 S3 and 1961-1968 for 256x448x64 (same GPU)
+    (8192, 8192, 8192, 1, 1): dict(block=(256, 512, 64), num_stages=4, cta_pair=True),
     # 144 tiles of 256x352 fill two waves of 76 pairs: 91.8-92.4 us vs 92.6-93.8 for 256x384x64 S4
     # (128 tiles); 94.2 vs 96.3 us with and without the evict-first hint; 100.1 for 256x224x64 S6
     (4000, 3000, 5000, 0, 2): dict(block=(256, 352, 64), num_stages=5, cta_pair=True, stream_operands=True),
