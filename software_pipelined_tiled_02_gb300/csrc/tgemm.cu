@@ -291,7 +291,12 @@ struct MmaCtx {
 // writes block_N / 2 columns further on); 1 otherwise.  Descriptors of slot s
 // are the slot-0 descriptors plus s slot strides (address field in 16-byte
 // units); k-step kk adds 32 bytes.  In pair mode this runs in the even CTA
-// only: its commits arrive on the barriers of both CTAs.
+// only: its commits arrive on the barriers of both CTAs.  The whole warp runs
+// the loop converged, and elect.sync inside each MMA and commit picks the lane
+// that issues it.  With lane 0 alone issuing under a branch, the issue path
+// took about 360 cycles per slot plus 69 per MMA (clock64 probe), more than the
+// tensor core's time for slots of under ~900 MMA cycles: 448 for a 256x224x64
+// pair tile, 704 for 256x352x64.  Elected issue takes about 35 per MMA.
 template <int NK, int MH, bool PAIR>
 __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volatile int *abort, int lane)
 {
@@ -308,9 +313,9 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
     };
     auto commit_both = [&](uint32_t bar) {
         if constexpr (PAIR)
-            mma_commit_pair(bar, uint16_t(0x3));
+            mma_commit_pair_elect(bar, uint16_t(0x3));
         else
-            mma_commit(bar);
+            mma_commit_elect(bar);
     };
     const uint64_t ad0 = smem_desc(c.sA, p), bd0 = smem_desc(c.sB, p);
     const uint64_t a_step = p.a_slot >> 4, b_step = p.b_slot >> 4;
@@ -348,7 +353,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
                           ((uint32_t(bd & 0x3FFFu) << 4) + p.b_slot) <= (c.sB & 0x3FFFFu) + uint32_t(S) * p.b_slot &&
                           (a + 1) * p.acc_cols <= p.tmem_cols && kb1 <= p.num_kb,
                       p, abort, 1, it);
-            if (lane == 0 && in_range) {
+            if (in_range) {
                 const uint32_t first = kb != kb0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < NK; ++kk) {
@@ -374,7 +379,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
             }
         }
         if (!ok) break;
-        if (lane == 0) commit_both(acc_full(a));  // accumulator a is complete (in both CTAs)
+        commit_both(acc_full(a));  // accumulator a is complete (in both CTAs)
         __syncwarp();
         if (++a == p.acc_stages) {
             a = 0;
@@ -894,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
             cluster_sync();
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer: the warp runs the loop, lane 0 drives the tensor core.
+        // ---------------- MMA issuer: the warp runs the loop, one elected lane drives the tensor core.
         // The k-steps per slot and the MMAs per k-step are compile-time in
         // the issue loop, so each MMA costs one descriptor add.
         if (!PAIR || rank == 0) {
