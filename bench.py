@@ -60,6 +60,8 @@ def parse_args(argv=None):
                     help="1: L2 evict-first hint on the operand loads (default: tuned table)")
     ap.add_argument("--grid-reduce", type=int, choices=(0, 1), default=None,
                     help="1: reduce K splits inside the GEMM kernel after a grid-wide barrier (default: tuned table)")
+    ap.add_argument("--multicast-b", type=int, choices=(0, 1), default=None,
+                    help="1: clusters of two CTA pairs share B through TMA multicast (default: tuned table)")
     ap.add_argument("--group-m", type=int, default=None,
                     help="M-blocks per raster group of the persistent schedule (default: tuned table; 0 = 8)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -152,13 +154,15 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
-def config_key(block, stages, pair, split_k, group_m=8, cluster_k=0, stream_operands=False, grid_reduce=False):
+def config_key(block, stages, pair, split_k, group_m=8, cluster_k=0, stream_operands=False, grid_reduce=False,
+               multicast_b=False):
     """The launch configuration as the ncu summaries record it."""
     key = (f"{block[0]},{block[1]},{block[2]} S{stages} pair{int(bool(pair))} split{int(split_k)} "
            f"group{int(group_m) or 8}")
     key += f" cluster{int(cluster_k)}" if cluster_k and cluster_k > 1 else ""
     key += " stream" if stream_operands else ""
-    return key + (" gridreduce" if grid_reduce else "")
+    key += " gridreduce" if grid_reduce else ""
+    return key + (" mcast" if multicast_b else "")
 
 
 def recorded_traffic(workload, config=None):
@@ -371,6 +375,7 @@ def run_ours(args, w, world, rank, local):
         cluster_k = args.cluster_k or 0
         stream_ops = bool(args.stream_operands)
         grid_red = bool(args.grid_reduce)
+        mcast = bool(args.multicast_b)
     else:
         cfg = tg.default_config(M, N, K, w["dtype"], w["out"])
         block, stages, pair, split_k = cfg["block"], cfg["num_stages"], cfg["cta_pair"], cfg["split_k"]
@@ -384,6 +389,7 @@ def run_ours(args, w, world, rank, local):
         cluster_k = cfg["cluster_k"] if args.cluster_k is None else args.cluster_k
         stream_ops = cfg["stream_operands"] if args.stream_operands is None else bool(args.stream_operands)
         grid_red = cfg["grid_reduce"] if args.grid_reduce is None else bool(args.grid_reduce)
+        mcast = cfg["multicast_b"] if args.multicast_b is None else bool(args.multicast_b)
     A, B = inputs.workload_operands(args.workload)
     hA = inputs.bits_to_torch(A, w["dtype"])
     hB = inputs.bits_to_torch(B, w["dtype"])
@@ -391,7 +397,7 @@ def run_ours(args, w, world, rank, local):
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[w["out"]]
     dC = torch.empty((M, N), dtype=tdt, device=dev)
     plan = tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k, group_m=group_m,
-                   cluster_k=cluster_k, stream_operands=stream_ops, grid_reduce=grid_red)
+                   cluster_k=cluster_k, stream_operands=stream_ops, grid_reduce=grid_red, multicast_b=mcast)
     info = plan.info
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -452,7 +458,7 @@ def run_ours(args, w, world, rank, local):
         pCs = [torch.empty((M, N), dtype=tdt).pin_memory() for _ in range(2)]
         plans = [plan, tg.Plan(M, N, K, w["dtype"], w["out"], block, stages, pair=pair, split_k=split_k,
                                group_m=group_m, cluster_k=cluster_k, stream_operands=stream_ops,
-                               grid_reduce=grid_red)]
+                               grid_reduce=grid_red, multicast_b=mcast)]
         bufs = [(dA, dB, dC), (torch.empty_like(dA), torch.empty_like(dB), torch.empty_like(dC))]
         streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
         torch.cuda.synchronize(dev)
@@ -510,7 +516,7 @@ def run_ours(args, w, world, rank, local):
                      "traffic": recorded_traffic(args.workload,
                                                  config_key(block, stages, pair, info["split_k"], group_m,
                                                             info["cluster_k"], info["stream_operands"],
-                                                            info["grid_reduce"])),
+                                                            info["grid_reduce"], info["multicast_b"])),
                      "kernel": ("tgemm_kernel + splitk_reduce_kernel, timed together per step"
                                 if two_kernels else "tgemm_kernel"),
                      "flops_per_launch": flops, "algorithmic_bytes_per_launch": algo_bytes})
@@ -527,7 +533,8 @@ def run_ours(args, w, world, rank, local):
                                split_k=int(info["split_k"]), group_m=int(group_m) or 8,
                                cluster_k=int(info["cluster_k"]),
                                stream_operands=int(info["stream_operands"]),
-                               grid_reduce=int(info["grid_reduce"])), "roofline": roofline,
+                               grid_reduce=int(info["grid_reduce"]),
+                               multicast_b=int(info["multicast_b"])), "roofline": roofline,
                 "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": args.steps * (2 if two_kernels else 1),
                 "clocks": clocks,

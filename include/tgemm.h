@@ -216,6 +216,23 @@ int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, in
  *     512 x 512 x 32768 case measured 33 us against 31.5 us with the second
  *     kernel: reading the partials costs the same either way and the barrier
  *     adds its own wait.  Other values: INVALID_ARG.
+ *   multicast_b: 0 = each CTA pair loads its own B rows.  1 = thread-block
+ *     clusters of four CTAs, two pairs that take the two M-adjacent tiles of
+ *     one N-block (the second pair's tile lies past M when the M-blocks are
+ *     odd in number; it loads zeros and stores nothing).  The CTAs of rank r
+ *     and r ^ 2 hold the same rows of B: each loads one part of them and TMA
+ *     multicast writes it into both, so each SM issues the copies of half its
+ *     B rows and L2 serves each B line once per cluster.  A slot is refilled
+ *     once both pairs' MMAs have finished with it.  Same MMAs in the same
+ *     order: results are bit-identical to cta_pair alone.  Requires
+ *     cta_pair = 1, no K split, stream_k, grid_reduce or cluster_k, and a
+ *     CTA's B box (block_N / 2, or block_N / 4 for a tile wider than 256) of
+ *     at least 16 rows (parts of whole 8-row swizzle atoms); else INVALID_ARG.
+ *     Clusters of four fit fewer at a time than pairs (36 on GB300, 144 SMs).
+ *     On GB300 it pays where B's rows straddle L2 lines: 4000 x 3000 x 5000
+ *     fp16 (a 10,000-byte row pitch) ran 83.4-83.9 us against 88.1-88.6 us
+ *     with pairs alone.  4096^3 and 8192^3 ran slower with it (their tiles
+ *     fill rounds of 36 clusters poorly).
  */
 typedef struct tgemm_plan_opts {
     int cta_pair;
@@ -226,6 +243,7 @@ typedef struct tgemm_plan_opts {
     int stream_operands;
     int grid_reduce;
     int stream_k;
+    int multicast_b;
 } tgemm_plan_opts;
 
 /* tgemm_validate with options (NULL = defaults): the option ranges above
@@ -312,6 +330,7 @@ typedef struct tgemm_plan_info {
     int stream_operands; /* 1: operand loads carry an L2 evict-first hint */
     int grid_reduce;     /* 1: K splits reduced in the GEMM kernel after a grid-wide barrier */
     int stream_k_tiles;  /* tiles of the stream-K tail (0: none) */
+    int multicast_b;     /* 1: clusters of two CTA pairs share B through TMA multicast */
 } tgemm_plan_info;
 
 int tgemm_get_plan_info(tgemm_plan_t plan, tgemm_plan_info *info);

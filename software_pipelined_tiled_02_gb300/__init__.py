@@ -48,7 +48,7 @@ class PlanInfo(ctypes.Structure):
                 ("smem_bound", ctypes.c_int64), ("smem_limit", ctypes.c_int), ("num_sms", ctypes.c_int),
                 ("cta_pair", ctypes.c_int), ("split_k", ctypes.c_int), ("num_units", ctypes.c_int),
                 ("prefetch", ctypes.c_int), ("cluster_k", ctypes.c_int), ("stream_operands", ctypes.c_int),
-                ("grid_reduce", ctypes.c_int), ("stream_k_tiles", ctypes.c_int)]
+                ("grid_reduce", ctypes.c_int), ("stream_k_tiles", ctypes.c_int), ("multicast_b", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -57,7 +57,7 @@ class PlanInfo(ctypes.Structure):
 class PlanOpts(ctypes.Structure):
     _fields_ = [("cta_pair", ctypes.c_int), ("group_m", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("prefetch", ctypes.c_int), ("cluster_k", ctypes.c_int), ("stream_operands", ctypes.c_int),
-                ("grid_reduce", ctypes.c_int), ("stream_k", ctypes.c_int)]
+                ("grid_reduce", ctypes.c_int), ("stream_k", ctypes.c_int), ("multicast_b", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -160,11 +160,11 @@ def tgemm_plan(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages)
 
 
 def tgemm_plan_ex(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, cta_pair=0, group_m=0,
-                  split_k=0, prefetch=0, cluster_k=0, stream_operands=0, grid_reduce=0, stream_k=0):
+                  split_k=0, prefetch=0, cluster_k=0, stream_operands=0, grid_reduce=0, stream_k=0, multicast_b=0):
     """Returns ``(status, handle)``; handle is None on failure."""
     h = ctypes.c_void_p()
     opts = PlanOpts(int(cta_pair), int(group_m), int(split_k), int(prefetch), int(cluster_k), int(stream_operands),
-                    int(grid_reduce), int(stream_k))
+                    int(grid_reduce), int(stream_k), int(multicast_b))
     rc = load().tgemm_plan_ex(ctypes.byref(h), M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K,
                               num_stages, ctypes.byref(opts))
     return int(rc), (h if rc == OK else None)
@@ -172,9 +172,9 @@ def tgemm_plan_ex(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stag
 
 def tgemm_validate_ex(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit, cta_pair=0,
                       group_m=0, split_k=0, prefetch=0, cluster_k=0, stream_operands=0, grid_reduce=0,
-                      stream_k=0) -> int:
+                      stream_k=0, multicast_b=0) -> int:
     opts = PlanOpts(int(cta_pair), int(group_m), int(split_k), int(prefetch), int(cluster_k), int(stream_operands),
-                    int(grid_reduce), int(stream_k))
+                    int(grid_reduce), int(stream_k), int(multicast_b))
     return int(load().tgemm_validate_ex(M, N, K, _dt(dtype), _dt(out_dtype), block_M, block_N, block_K,
                                         num_stages, smem_limit, ctypes.byref(opts)))
 
@@ -239,21 +239,23 @@ class Plan:
 
     def __init__(self, M, N, K, dtype="f16", out_dtype=None, block=(128, 256, 64), num_stages=4, pair=False,
                  split_k=1, prefetch=0, group_m=0, cluster_k=0, stream_operands=False, grid_reduce=False,
-                 stream_k=False):
+                 stream_k=False, multicast_b=False):
         dtype = _dt(dtype)
         out_dtype = dtype if out_dtype is None else _dt(out_dtype)
         bm, bn, bk = block
-        if pair or split_k > 1 or prefetch or group_m or cluster_k > 1 or stream_operands or grid_reduce or stream_k:
+        if (pair or split_k > 1 or prefetch or group_m or cluster_k > 1 or stream_operands or grid_reduce or stream_k
+                or multicast_b):
             rc, h = tgemm_plan_ex(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages, cta_pair=int(bool(pair)),
                                   split_k=int(split_k), prefetch=int(prefetch), group_m=int(group_m),
                                   cluster_k=int(cluster_k), stream_operands=int(bool(stream_operands)),
-                                  grid_reduce=int(bool(grid_reduce)), stream_k=int(bool(stream_k)))
+                                  grid_reduce=int(bool(grid_reduce)), stream_k=int(bool(stream_k)),
+                                  multicast_b=int(bool(multicast_b)))
         else:
             rc, h = tgemm_plan(M, N, K, dtype, out_dtype, bm, bn, bk, num_stages)
         if rc != OK:
             raise TgemmError(rc, f"tgemm_plan(M={M}, N={N}, K={K}, block={block}, num_stages={num_stages}, "
                                  f"pair={pair}, split_k={split_k}, cluster_k={cluster_k}, "
-                                 f"stream_operands={stream_operands})")
+                                 f"stream_operands={stream_operands}, multicast_b={multicast_b})")
         self.pair = bool(pair)
         self.split_k = int(split_k)
         self.cluster_k = int(cluster_k)
@@ -351,14 +353,14 @@ _PLANS_MAX = 64
 
 def default_config(M, N, K, dtype="f16", out_dtype=None) -> dict:
     """The tuned default {block, num_stages, cta_pair, split_k, group_m, cluster_k, stream_operands,
-    grid_reduce, stream_k} for a shape."""
+    grid_reduce, stream_k, multicast_b} for a shape."""
     from . import defaults
 
     return defaults.choose(M, N, K, _dt(dtype), _dt(dtype) if out_dtype is None else _dt(out_dtype))
 
 
 def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=None, pair=None, split_k=None,
-         group_m=None, cluster_k=None, stream_operands=None, grid_reduce=None, stream_k=None):
+         group_m=None, cluster_k=None, stream_operands=None, grid_reduce=None, stream_k=None, multicast_b=None):
     """``A[M,K] . B[N,K]^T`` on the GPU through ``libtgemm.so``.
 
     ``out_dtype`` defaults to the operand dtype; ``torch.float32`` returns the
@@ -386,8 +388,9 @@ def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=Non
     stream_operands = bool(cfg["stream_operands"] if stream_operands is None else stream_operands)
     grid_reduce = bool(cfg["grid_reduce"] if grid_reduce is None else grid_reduce)
     stream_k = bool(cfg["stream_k"] if stream_k is None else stream_k)
+    multicast_b = bool(cfg["multicast_b"] if multicast_b is None else multicast_b)
     key = (M, N, K, dt, odt, tuple(block), num_stages, pair, split_k, group_m, cluster_k, stream_operands,
-           grid_reduce, stream_k, A.device.index)
+           grid_reduce, stream_k, multicast_b, A.device.index)
     # The cache lock covers the lookup only; the enqueue holds the plan's own
     # lock (a plan caches tensor maps per pointer triple, so one host thread
     # at a time), so threads running different plans do not serialise.
@@ -397,7 +400,7 @@ def gemm(A, B, out_dtype=None, block=None, num_stages=None, out=None, stream=Non
             if plan is None:
                 plan = _plans[key] = Plan(M, N, K, dt, odt, block, num_stages, pair=pair, split_k=split_k,
                                           group_m=group_m, cluster_k=cluster_k, stream_operands=stream_operands,
-                                          grid_reduce=grid_reduce, stream_k=stream_k)
+                                          grid_reduce=grid_reduce, stream_k=stream_k, multicast_b=multicast_b)
                 while len(_plans) > _PLANS_MAX:
                     victim = _plans.popitem(last=False)[1]
                     with victim.lock:  # waits for an enqueue in progress on it

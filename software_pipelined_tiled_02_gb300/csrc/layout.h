@@ -156,8 +156,22 @@ inline bool csplit_supported(int bm, int bn, int pair, int eff_splits, int csk)
     return bn % csk == 0 && (bn / csk) % kEpiCols == 0 && bn / csk <= 128;
 }
 
+// B shared by two CTA pairs (kernel mode 3, clusters of 4): the pairs take
+// M-adjacent tiles of one N-block, so the CTAs of rank r and r ^ 2 hold the
+// same rows of B.  Each loads one part of its B box and multicasts it to both:
+// rows [0, part0) from the first pair, [part0, b_box_rows) from the second,
+// each part a whole number of 8-row swizzle atoms.
+inline int mcast_part0(int b_box_rows) { return (b_box_rows / 2 + 7) / 8 * 8; }
+inline bool mcast_supported(int bm, int bn, int pair, int eff_splits, int csk)
+{
+    if (!pair || bm != 256 || eff_splits != 1 || csk > 1) return false;
+    const int box = bn > 256 ? bn / 4 : bn / 2;  // a CTA's rows of one B box (per N-half)
+    const int p0 = mcast_part0(box);
+    return box % 8 == 0 && p0 >= 8 && box - p0 >= 8;
+}
+
 inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int bm, int bn, int bk,
-                    int stages, int64_t smem_limit, int pair = 0, int splits = 1, int csk = 0)
+                    int stages, int64_t smem_limit, int pair = 0, int splits = 1, int csk = 0, int mcast = 0)
 {
     if (dtype != kF16 && dtype != kBF16) return kErrUnsupportedDtype;
     if (out_dtype != kF32 && out_dtype != dtype) return kErrUnsupportedDtype;
@@ -179,6 +193,9 @@ inline int validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, i
     if (((M + bm - 1) / bm) * ((N + bn - 1) / bn) * int64_t(eff) > kMaxUnits) return kErrInvalidArg;
     if (stages > 64) return kErrSmemBudget;  // keeps the layout arithmetic in 32 bits
     if (csk > 1 && !csplit_supported(bm, bn, pair, eff, csk)) return kErrInvalidArg;
+    // The last M-block pair of an odd tile count has a second tile past M: its
+    // rows, up to one more 256-row block, are still 32-bit TMA coordinates.
+    if (mcast && (!mcast_supported(bm, bn, pair, eff, csk) || M > kMaxDim - 512)) return kErrInvalidArg;
     // A split-K kernel that reduces through the workspace stages fp32 partial
     // tiles whatever the final output type.
     const int staged = eff > 1 && csk <= 1 ? kF32 : out_dtype;

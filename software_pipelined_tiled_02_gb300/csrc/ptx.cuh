@@ -271,6 +271,32 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void *
         : "memory");
 }
 
+// tma_load_2d_pair multicast: the box is written at the same offset into the
+// shared memory of every CTA in `cta_mask`, and each copy completes the
+// transaction count of the mbarrier at `bar_cluster`'s offset in the even CTA
+// of the receiving CTA's pair (`bar_cluster` is the issuing pair's even-CTA
+// barrier).  Issued by one thread.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void *tmap, int32_t x, int32_t y,
+                                                    uint32_t bar_cluster, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster), "h"(cta_mask)
+        : "memory");
+}
+
+// tma_load_2d_pair_mc with an L2 cache policy for the lines it reads.
+__device__ __forceinline__ void tma_load_2d_pair_mc_hint(uint32_t dst, const void *tmap, int32_t x, int32_t y,
+                                                         uint32_t bar_cluster, uint16_t cta_mask, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster), "h"(cta_mask), "l"(policy)
+        : "memory");
+}
+
 // Pair-wide TMEM allocation: one warp of each CTA of the pair executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols)
 {

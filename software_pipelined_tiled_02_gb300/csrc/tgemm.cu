@@ -66,6 +66,7 @@ namespace tg {
 
 struct Params {  // 64-byte aligned through its CUtensorMap members
     CUtensorMap tmA, tmB, tmC;
+    CUtensorMap tmB1;           // mode 3: B's second multicast part (rows part0 .. b_box_rows)
     int M, N, K;
     int num_kb;                 // ceil(K / bk)
     int tiles_m, tiles_n, num_tiles, group_m;
@@ -122,6 +123,10 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
     int sk_rows;                // rows of a tile one CTA holds (its part of a stream-K partial)
     float *sk_ws;               // [workers][2][ranks][sk_rows][bn] fp32 partial pieces
     int *sk_cnt;                // [sk_tiles][ranks] arrival counts, zero between launches
+    // M-blocks of the persistent schedule: tiles_m, or in mode 3 (two CTA pairs
+    // per cluster sharing B) ceil(tiles_m / 2) blocks of two M-adjacent tiles.
+    int sched_m;
+    int b_part0;                // mode 3: rows of B's first multicast part (tmB's box)
 };
 
 // ---------------------------------------------------------------- device side
@@ -195,7 +200,7 @@ __device__ __forceinline__ void tile_coords(const Params &p, int t, int &m_blk, 
     const int group_tiles = p.group_m * p.tiles_n;
     const int g = t / group_tiles;
     const int first_m = g * p.group_m;
-    const int gm = min(p.group_m, p.tiles_m - first_m);
+    const int gm = min(p.group_m, p.sched_m - first_m);
     const int r = t - g * group_tiles;
     m_blk = first_m + r % gm;
     n_blk = r / gm;
@@ -281,6 +286,9 @@ struct MmaCtx {
     int S;
     uint32_t stall, drain;
     int unit0, ustride;  // first tile and tile stride of this CTA (or CTA pair)
+    // pair mode: CTAs whose barriers a commit arrives on -- every CTA that
+    // loads into this pair's slots (empty), the pair (acc_full), this CTA (drain)
+    uint16_t empty_mask, pair_mask, self_mask;
 };
 
 // The MMA warp's main loop.  NK = MMAs of K = 16 per ring slot (block_K / 16),
@@ -311,9 +319,9 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
         else
             mma_f16(d, ad, bd, p.idesc, acc);
     };
-    auto commit_both = [&](uint32_t bar) {
+    auto commit_both = [&](uint32_t bar, uint16_t mask) {
         if constexpr (PAIR)
-            mma_commit_pair_elect(bar, uint16_t(0x3));
+            mma_commit_pair_elect(bar, mask);
         else
             mma_commit_elect(bar);
     };
@@ -364,7 +372,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
                     for (int h = 0; h < MH; ++h)
                         mma(h ? d2 : d, ad + ka + (h ? a_half : 0), bd + kb_ + (h ? b_half : 0), kk == 0 ? first : 1u);
                 }
-                commit_both(empty(s));  // slot s (in both CTAs) may be refilled once these MMAs finish
+                commit_both(empty(s), c.empty_mask);  // slot s may be refilled once these MMAs finish
             }
             __syncwarp();
             ++it;
@@ -379,7 +387,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
             }
         }
         if (!ok) break;
-        commit_both(acc_full(a));  // accumulator a is complete (in both CTAs)
+        commit_both(acc_full(a), c.pair_mask);  // accumulator a is complete (in both CTAs)
         __syncwarp();
         if (++a == p.acc_stages) {
             a = 0;
@@ -389,7 +397,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const MmaCtx &c, volat
     // Every MMA this warp issued must finish before TMEM is freed.
     if (lane == 0) {
         if constexpr (PAIR)
-            mma_commit_pair(c.drain, uint16_t(0x1));
+            mma_commit_pair(c.drain, c.self_mask);
         else
             mma_commit(c.drain);
         wait_bar(c.drain, 0, p, abort, 1, it, false);
@@ -715,8 +723,9 @@ __device__ __noinline__ void csplit_epilogue(const Params &p, uint32_t sA, int *
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constant__ Params p)
 {
-    constexpr bool PAIR = MODE == 1;
+    constexpr bool PAIR = MODE == 1 || MODE == 3;
     constexpr bool CSPLIT = MODE == 2;
+    constexpr bool MC = MODE == 3;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = (kSmemAlign - (raw & (kSmemAlign - 1))) & (kSmemAlign - 1);
@@ -741,14 +750,25 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
 
     const int warp = int(threadIdx.x) / 32;
     const int lane = int(threadIdx.x) % 32;
-    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0: the pair's MMA-issuing CTA
-    const int unit0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
-    const int ustride = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
+    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;  // rank in the cluster
+    const uint32_t rank = MC ? crank & 1u : crank;         // in the pair; 0: the MMA-issuing CTA
+    const uint32_t leader = MC ? crank & ~1u : 0u;         // the pair's even CTA
+    const int pidx = MC ? int(crank >> 1) : 0;             // mode 3: the cluster's first or second pair
+    const int unit0 = MC ? int(blockIdx.x >> 2) : PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
+    const int ustride = MC ? int(gridDim.x >> 2) : PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
+    // A work item's tile: in mode 3 the cluster's item is a pair of M-adjacent
+    // tiles, the second pair taking the lower one (past M when tiles_m is odd:
+    // its A loads read zeros and its rows are not stored).
+    auto item = [&](int i, Unit &u) -> bool {
+        if (!work_item(p, unit0, i, u)) return false;
+        if constexpr (MC) u.mb = 2 * u.mb + pidx;
+        return true;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), 1);
+            mbar_init(empty(s), MC ? 2 : 1);  // mode 3: both pairs release a slot before it refills
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(acc_full(a), 1);
@@ -787,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         // Pair mode: each CTA loads its own rows of A and B into its own slot;
         // both complete the even CTA's full[s], which the even CTA arms with
         // the bytes of both.
-        const uint32_t full_leader = PAIR ? map_to_rank(full(0), 0) : 0u;
+        const uint32_t full_leader = PAIR ? map_to_rank(full(0), leader) : 0u;
         // Streamed operands: each line is read by the tiles that share it at
         // about the same time and not again, so it goes first when L2 needs room.
         const uint64_t policy = p.stream_ops ? policy_evict_first() : 0ull;
@@ -803,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         uint32_t phd = 0;
         for (int i = 0; ok; ++i) {
             Unit w;
-            if (!work_item(p, unit0, i, w)) break;
+            if (!item(i, w)) break;
             const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn + int(rank) * p.b_box_rows;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 if (!warp_wait(empty(s), ph ^ 1u, p, abort, 0, issued)) {
@@ -821,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                     }
                 }
                 const bool in_range =
-                    check(s < S && (kb * p.bk * 2) % 16 == 0 && kb < p.num_kb && w.mb < p.tiles_m &&
+                    check(s < S && (kb * p.bk * 2) % 16 == 0 && kb < p.num_kb && w.mb < (MC ? 2 * p.sched_m : p.tiles_m) &&
                               w.nb < p.tiles_n && int(p.panels) * int(p.a_panel16 << 4) <= int(p.a_slot) &&
                               int(p.panels) * int(p.b_panel16 << 4) <= int(p.b_slot),
                           p, abort, 0, issued);
@@ -836,7 +856,26 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                             const uint32_t b_at = b_dst + (uint32_t(pl) * p.b_panel16 << 4);
                             // a wide tile's second N-half: this CTA's rows of it, block_N / 2 further on
                             const uint32_t b2_at = b_dst + ((uint32_t(pl) * p.b_panel16 + p.b_half16) << 4);
-                            if (p.stream_ops) {
+                            if constexpr (MC) {
+                                // B: this CTA's part of its rows, multicast to it and to the CTA of
+                                // the other pair that holds the same rows (rank ^ 2)
+                                const uint32_t part = pidx ? uint32_t(p.b_part0) * p.row_bytes : 0u;
+                                const int yp = pidx ? p.b_part0 : 0;
+                                const void *bmap = pidx ? &p.tmB1 : &p.tmB;
+                                const uint16_t mask = uint16_t((1u << crank) | (1u << (crank ^ 2u)));
+                                if (p.stream_ops) {
+                                    tma_load_2d_pair_hint(a_at, &p.tmA, x, m0, fb, policy);
+                                    tma_load_2d_pair_mc_hint(b_at + part, bmap, x, n0 + yp, fb, mask, policy);
+                                    if (p.n_halves == 2)
+                                        tma_load_2d_pair_mc_hint(b2_at + part, bmap, x, n0 + (p.bn >> 1) + yp, fb, mask,
+                                                                 policy);
+                                } else {
+                                    tma_load_2d_pair(a_at, &p.tmA, x, m0, fb);
+                                    tma_load_2d_pair_mc(b_at + part, bmap, x, n0 + yp, fb, mask);
+                                    if (p.n_halves == 2)
+                                        tma_load_2d_pair_mc(b2_at + part, bmap, x, n0 + (p.bn >> 1) + yp, fb, mask);
+                                }
+                            } else if (p.stream_ops) {
                                 tma_load_2d_pair_hint(a_at, &p.tmA, x, m0, fb, policy);
                                 tma_load_2d_pair_hint(b_at, &p.tmB, x, n0, fb, policy);
                                 if (p.n_halves == 2) tma_load_2d_pair_hint(b2_at, &p.tmB, x, n0 + (p.bn >> 1), fb, policy);
@@ -872,8 +911,10 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         }
         if (!ok && lane == 0) {
             // Let the loads still in flight land before the CTA may exit:
-            // only the last min(S, issued) slots can be outstanding.
-            if (!PAIR || rank == 0) {
+            // only the last min(S, issued) slots can be outstanding.  In mode 3
+            // a CTA's B copies also land in the other pair, whose barriers it
+            // cannot wait on: every CTA takes the fixed wait below.
+            if (!MC && (!PAIR || rank == 0)) {
                 const int first = issued > S ? issued - S : 0;
                 for (int j = first; j < issued; ++j)
                     wait_bar(full(j % S), uint32_t((j / S) & 1), p, abort, 0, j, false);
@@ -903,7 +944,9 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         // The k-steps per slot and the MMAs per k-step are compile-time in
         // the issue loop, so each MMA costs one descriptor add.
         if (!PAIR || rank == 0) {
-            const MmaCtx c{sA, sB, tmem, bars, S, stall, drain, unit0, ustride};
+            const uint16_t pm = uint16_t(0x3u << leader);
+            const MmaCtx c{sA, sB, tmem, bars, S, stall, drain, unit0, ustride, uint16_t(MC ? 0xFu : 0x3u), pm,
+                           uint16_t(0x1u << leader)};
             if (p.mma_per_kstep == 2)
                 mma_dispatch_nk<2, PAIR>(p, c, abort, lane);
             else
@@ -943,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         bool sk_ok = true;
         for (int i = 0;; ++i, ++tiles_done) {
             Unit w;
-            if (!work_item(p, unit0, i, w)) break;
+            if (!item(i, w)) break;
             const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn;
             if (!warp_wait(acc_full(a), aph, p, abort, 2, tiles_done)) break;
             tc_fence_after();
@@ -1106,7 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
             __syncwarp();
             if (lane == 0) {
                 if constexpr (PAIR)
-                    mbar_arrive_cluster(map_to_rank(acc_empty(a), 0));
+                    mbar_arrive_cluster(map_to_rank(acc_empty(a), leader));
                 else
                     mbar_arrive(acc_empty(a));
             }
@@ -1246,6 +1289,7 @@ struct tgemm_plan_s {
     int smem_launch;
     int tiles_m, tiles_n, num_tiles, grid, group_m;
     int pair;  // clusters of two CTAs per block_M = 256 tile
+    int mc;    // clusters of two pairs sharing B through multicast (kernel mode 3)
     int splits;                // K splits (1: none)
     int csk;                   // > 1: splits reduced inside the kernel by clusters of csk CTAs
     float *d_work;             // split-K partial sums: splits (or, with csk, splits / csk) x M x N fp32
@@ -1277,7 +1321,8 @@ static int allow_max_smem(int dev, int limit)
     if (dev >= 0 && dev < 64 && done[dev]) return kOk;
     if (cudaFuncSetAttribute(tgemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess ||
         cudaFuncSetAttribute(tgemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess ||
-        cudaFuncSetAttribute(tgemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess) {
+        cudaFuncSetAttribute(tgemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess ||
+        cudaFuncSetAttribute(tgemm_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess) {
         cudaGetLastError();
         return kErrCuda;
     }
@@ -1298,6 +1343,7 @@ static void fill_params(Params &q, const Layout &L, int64_t M, int64_t N, int64_
     q.K = int(K);
     q.num_kb = int((K + block_K - 1) / block_K);
     q.tiles_m = tiles_m;
+    q.sched_m = tiles_m;
     q.tiles_n = tiles_n;
     q.num_tiles = tiles_m * tiles_n;
     q.group_m = group_m;
@@ -1383,9 +1429,13 @@ static int encode_maps(Params &q, const Layout &L, int dtype, int out_dtype, con
         const uint32_t box_k = uint32_t(L.swizzle_bytes / L.in_bytes);  // one K-panel per box
         const uint64_t pitch = K * uint64_t(L.in_bytes);
         rc = encode_2d(&q.tmA, dtype, A, K, M, pitch, box_k, uint32_t(L.a_rows), swz, operand_promotion(pitch));
+        // mode 3: B comes in two multicast parts, rows [0, b_part0) and [b_part0, b_box_rows)
+        const uint32_t b_box = uint32_t(L.b_rows / L.n_halves);
+        const uint32_t part0 = q.b_part0 > 0 ? uint32_t(q.b_part0) : b_box;
         if (rc == kOk)
-            rc = encode_2d(&q.tmB, dtype, B, K, N, pitch, box_k, uint32_t(L.b_rows / L.n_halves), swz,
-                           operand_promotion(pitch));
+            rc = encode_2d(&q.tmB, dtype, B, K, N, pitch, box_k, part0, swz, operand_promotion(pitch));
+        if (rc == kOk && q.b_part0 > 0)
+            rc = encode_2d(&q.tmB1, dtype, B, K, N, pitch, box_k, b_box - part0, swz, operand_promotion(pitch));
     }
     if (rc != kOk) return rc;
     // one store box per epilogue chunk: kEpiCols columns of one warp's accumulator rows
@@ -1413,6 +1463,9 @@ static int check_opts(const tgemm_plan_opts *opts, int num_stages)
     if (opts->grid_reduce != 0 && opts->grid_reduce != 1) return kErrInvalidArg;
     if (opts->stream_k != 0 && opts->stream_k != 1) return kErrInvalidArg;
     if (opts->stream_k && (opts->split_k > 1 || opts->cluster_k > 1)) return kErrInvalidArg;
+    if (opts->multicast_b != 0 && opts->multicast_b != 1) return kErrInvalidArg;
+    if (opts->multicast_b && (!opts->cta_pair || opts->stream_k || opts->grid_reduce || opts->cluster_k > 1))
+        return kErrInvalidArg;
     return kOk;
 }
 
@@ -1472,7 +1525,7 @@ int tgemm_validate_ex(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
     if (rc != kOk) return rc;
     return validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, smem_limit,
                     opts ? opts->cta_pair : 0, opts && opts->split_k > 1 ? opts->split_k : 1,
-                    opts && opts->cluster_k > 1 ? opts->cluster_k : 0);
+                    opts && opts->cluster_k > 1 ? opts->cluster_k : 0, opts ? opts->multicast_b : 0);
 }
 
 int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, int block_M, int block_N,
@@ -1490,8 +1543,10 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     if (check_opts(opts, num_stages) != kOk) return kErrInvalidArg;
     const int splits = effective_splits(K, block_K, opts && opts->split_k > 1 ? opts->split_k : 1);
     const int csk = opts && opts->cluster_k > 1 ? opts->cluster_k : 0;
+    const int mc = opts && opts->multicast_b ? 1 : 0;
     // Argument checks that need no device come first.
-    int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX, pair, splits, csk);
+    int rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, INT64_MAX, pair, splits, csk,
+                      mc);
     if (rc != kOk) return rc;
     int dev = 0, major = 0, minor = 0, sms = 0, limit = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
@@ -1503,7 +1558,7 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
         return kErrCuda;
     }
     if (major != 10 || minor != 3) return kErrArch;
-    rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit, pair, splits, csk);
+    rc = validate(M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, limit, pair, splits, csk, mc);
     if (rc != kOk) return rc;
 
     tgemm_plan_s *p = new (std::nothrow) tgemm_plan_s();
@@ -1517,6 +1572,7 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     // tiles and the reduction converts.
     p->L = make_layout(block_M, block_N, block_K, num_stages, dtype, splits > 1 && !csk ? kF32 : out_dtype, pair);
     p->pair = pair;
+    p->mc = mc;
     p->splits = splits;
     p->csk = csk;
     p->d_work = nullptr;
@@ -1555,7 +1611,30 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
         delete p;
         return kErrCuda;
     }
-    if (pair) {
+    if (mc) {
+        // Persistent clusters of two pairs, as many as can be resident at once;
+        // a cluster's work item is two M-adjacent tiles of one N-block.
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 4;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        const int items = (p->tiles_m + 1) / 2 * p->tiles_n;
+        cfg.gridDim = dim3(unsigned(4 * (items < sms / 4 ? items : sms / 4)), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = size_t(p->smem_launch);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, tgemm_kernel<3>, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            cudaFree(p->d_status);
+            delete p;
+            return kErrCuda;
+        }
+        p->grid = 4 * (items < clusters ? items : clusters);
+    } else if (pair) {
         // Persistent pairs: as many clusters of two as can be resident at once.
         cudaLaunchConfig_t cfg{};
         cudaLaunchAttribute attr[1];
@@ -1662,7 +1741,12 @@ int tgemm_plan_ex(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype,
     Params &q = p->params;
     fill_params(q, p->L, M, N, K, dtype, out_dtype, block_M, block_N, block_K, num_stages, pair, splits,
                 opts && opts->prefetch > 0 ? opts->prefetch : num_stages, p->group_m, p->tiles_m, p->tiles_n,
-                pair ? p->grid / 2 : p->grid, csk);
+                mc ? p->grid / 4 : pair ? p->grid / 2 : p->grid, csk);
+    if (mc) {
+        q.sched_m = (p->tiles_m + 1) / 2;
+        q.num_units = q.sched_m * p->tiles_n;  // work items: pairs of M-adjacent tiles
+        q.b_part0 = mcast_part0(q.b_box_rows);
+    }
     q.watchdog_ns = p->watchdog_ns;
     q.status = p->d_status;
     q.ws = p->d_work;
@@ -1715,7 +1799,7 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
         unsigned na = 0;
         if (p->pair || p->csk) {
             attr[na].id = cudaLaunchAttributeClusterDimension;
-            attr[na].val.clusterDim.x = p->csk ? unsigned(p->csk) : 2u;
+            attr[na].val.clusterDim.x = p->csk ? unsigned(p->csk) : p->mc ? 4u : 2u;
             attr[na].val.clusterDim.y = 1;
             attr[na].val.clusterDim.z = 1;
             ++na;
@@ -1731,7 +1815,11 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
         cfg.stream = reinterpret_cast<cudaStream_t>(stream);
         cfg.attrs = attr;
         cfg.numAttrs = na;
-        if (cudaLaunchKernelEx(&cfg, p->csk ? tgemm_kernel<2> : p->pair ? tgemm_kernel<1> : tgemm_kernel<0>,
+        if (cudaLaunchKernelEx(&cfg,
+                               p->csk  ? tgemm_kernel<2>
+                               : p->mc ? tgemm_kernel<3>
+                               : p->pair ? tgemm_kernel<1>
+                                         : tgemm_kernel<0>,
                                p->params) != cudaSuccess) {
             cudaGetLastError();
             return kErrCuda;
@@ -1848,6 +1936,7 @@ int tgemm_get_plan_info(tgemm_plan_t p, tgemm_plan_info *info)
     info->stream_operands = p->params.stream_ops;
     info->grid_reduce = p->grid_reduce;
     info->stream_k_tiles = p->sk_tiles;
+    info->multicast_b = p->mc;
     return kOk;
 }
 

@@ -17,17 +17,20 @@ from __future__ import annotations
 # cta_pair, split_k (K splits), group_m (the persistent raster's group of
 # M-blocks; 0: the library's 8), cluster_k (> 1: K splits reduced inside the
 # kernel by clusters of that many CTAs), stream_operands (L2 evict-first
-# hint on the operand loads) and grid_reduce (K splits reduced in the GEMM
-# kernel after a grid-wide barrier).  The comments give same-GPU, interleaved timings
+# hint on the operand loads), grid_reduce (K splits reduced in the GEMM
+# kernel after a grid-wide barrier) and multicast_b (clusters of two CTA
+# pairs that share B through TMA multicast).  The comments give same-GPU, interleaved timings
 # against the runner-up.
 FROZEN = {
     # 1643 vs 1607 TFLOP/s for one CTA 256x224x64, group 8
     (4096, 4096, 4096, 0, 0): dict(block=(256, 224, 128), num_stages=3, cta_pair=True, group_m=2),
     # 1952-1976 vs 1897-1922 for pair 256x256x128 S3 and 1961-1968 for 256x448x64 (same GPU)
     (8192, 8192, 8192, 1, 1): dict(block=(256, 512, 64), num_stages=4, cta_pair=True),
-    # 144 tiles of 256x352 fill two waves of 76 pairs: 91.8-92.4 us vs 92.6-93.8 for 256x384x64 S4
-    # (128 tiles); 94.2 vs 96.3 us with and without the evict-first hint; 100.1 for 256x224x64 S6
-    (4000, 3000, 5000, 0, 2): dict(block=(256, 352, 64), num_stages=5, cta_pair=True, stream_operands=True),
+    # 144 tiles of 256x352 fill two waves of 76 pairs, or with B shared by two pairs (multicast) 72
+    # work items on 36 clusters of four: 84.0 us vs 88.9 for the pairs alone (same GPU), 89.1 for
+    # 256x384x64 S4 with multicast; the 10,000-byte row pitch makes each B row two L2 requests
+    (4000, 3000, 5000, 0, 2): dict(block=(256, 352, 64), num_stages=5, cta_pair=True, stream_operands=True,
+                                   multicast_b=True),
     # 31.2 vs 33.3 us without the evict-first hint; 35.4 for 128x128x64 S6 split 9; 166 unsplit;
     # the in-kernel cluster reduction (128x256x64 S4, split 16, clusters of 4) 38.9;
     # the reduction in the GEMM kernel after a grid-wide barrier 33.3
@@ -37,7 +40,7 @@ FROZEN = {
 }
 
 DEFAULT_OPTS = dict(cta_pair=False, split_k=1, group_m=0, cluster_k=0, stream_operands=False, grid_reduce=False,
-                    stream_k=False)
+                    stream_k=False, multicast_b=False)
 
 # Candidate tiles: (block, depth, relative steady-state throughput per SM,
 # CTA pair), measured on GB300 at whole waves.  A pair computes one 256-row

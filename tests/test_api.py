@@ -48,7 +48,8 @@ C_PROGRAM = r"""
 
 int main(void)
 {
-    tgemm_plan_opts opts = {1, 2, 1, 0, 0, 0, 0, 0};  /* pair, group, split, prefetch, cluster, stream, grid, stream-K */
+    /* pair, group, split, prefetch, cluster, stream, grid, stream-K, multicast B */
+    tgemm_plan_opts opts = {1, 2, 1, 0, 0, 0, 0, 0, 0};
     int64_t bound = tgemm_smem_bound(TGEMM_F16, 128, 128, 32, 3);
     int one = tgemm_validate(4096, 4096, 4096, TGEMM_F16, TGEMM_F16, 256, 224, 64, 3, 232448);
     int pair = tgemm_validate_ex(4096, 4096, 4096, TGEMM_F16, TGEMM_F16, 256, 224, 128, 3, 232448, &opts);
@@ -210,6 +211,29 @@ def test_validate_ex_stream_k_rules(lib):
     assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 4, L, split_k=2, stream_k=1) == tg.ERR_INVALID_ARG
     assert V(512, 512, 32768, tg.F16, tg.F32, 128, 256, 64, 4, L, split_k=8, cluster_k=4,
              stream_k=1) == tg.ERR_INVALID_ARG
+
+
+def test_validate_ex_multicast_rules(lib):
+    V = tg.tgemm_validate_ex
+    L = LIMIT_227K
+    assert V(4000, 3000, 5000, tg.F16, tg.F32, 256, 352, 64, 5, L, cta_pair=1, multicast_b=1) == tg.OK
+    assert V(4000, 3000, 5000, tg.F16, tg.F32, 256, 352, 64, 5, L, cta_pair=1, multicast_b=2) == tg.ERR_INVALID_ARG
+    # two CTA pairs per cluster: pairs only, one K split, no stream-K tail or in-kernel reduction
+    assert V(4000, 3000, 5000, tg.F16, tg.F32, 256, 352, 64, 5, L, multicast_b=1) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 32768, tg.F16, tg.F32, 256, 256, 128, 3, L, cta_pair=1, split_k=19,
+             multicast_b=1) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 32768, tg.F16, tg.F32, 256, 256, 128, 3, L, cta_pair=1, split_k=1, multicast_b=1) == tg.OK
+    assert V(4000, 3000, 5000, tg.F16, tg.F32, 256, 352, 64, 5, L, cta_pair=1, stream_k=1,
+             multicast_b=1) == tg.ERR_INVALID_ARG
+    assert V(512, 512, 4096, tg.F16, tg.F32, 256, 256, 64, 4, L, cta_pair=1, split_k=2, grid_reduce=1,
+             multicast_b=1) == tg.ERR_INVALID_ARG
+    # the smallest pair tile: a 16-row B box in two 8-row parts
+    assert V(512, 64, 512, tg.F16, tg.F16, 256, 32, 64, 4, L, cta_pair=1, multicast_b=1) == tg.OK
+    # the second tile of the last cluster may lie one 256-row block past M: M stays 512 below the limit
+    big = (1 << 31) - 1 - 256
+    assert V(big - 512, 64, 64, tg.F16, tg.F16, 256, 32, 64, 4, L, cta_pair=1, multicast_b=1) == tg.OK
+    assert V(big - 511, 64, 64, tg.F16, tg.F16, 256, 32, 64, 4, L, cta_pair=1, multicast_b=1) == tg.ERR_INVALID_ARG
+    assert V(big - 511, 64, 64, tg.F16, tg.F16, 256, 32, 64, 4, L, cta_pair=1) == tg.OK
 
 
 def stream_k_tail(T, G, KB):

@@ -93,6 +93,8 @@ def test_recorded_traffic_requires_same_launch_config(tmp_path, monkeypatch):
     key = bench.config_key((256, 224, 64), 3, False, 1)
     assert key == "256,224,64 S3 pair0 split1 group8"
     assert bench.config_key((256, 224, 64), 3, False, 1, 4) == "256,224,64 S3 pair0 split1 group4"
+    assert (bench.config_key((256, 352, 64), 5, True, 1, 8, 0, True, False, True) ==
+            "256,352,64 S5 pair1 split1 group8 stream mcast")
     p = tmp_path / "tgemm_kernel_wl.md"
     p.write_text(f"- kernel_source_sha256: `{bench.kernel_source_hash()}`\n- config: `{key}`\n"
                  "- dram_bytes_per_launch: 99\n")

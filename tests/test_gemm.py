@@ -24,11 +24,12 @@ def to_dev(bits, dtype):
     return inputs.bits_to_torch(bits, dtype).cuda()
 
 
-def run(tg, A, B, dtype, out, block, stages, pair=False, split_k=1, group_m=0, cluster_k=0):
+def run(tg, A, B, dtype, out, block, stages, pair=False, split_k=1, group_m=0, cluster_k=0, stream_operands=False,
+        multicast_b=False):
     M, K = A.shape
     N = B.shape[0]
     plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair, split_k=split_k, group_m=group_m,
-                   cluster_k=cluster_k)
+                   cluster_k=cluster_k, stream_operands=stream_operands, multicast_b=multicast_b)
     dA, dB = to_dev(A, dtype), to_dev(B, dtype)
     C = torch.full((M, N), float("nan"), dtype=TORCH[out], device="cuda")
     plan.run(dA, dB, C)
@@ -159,6 +160,62 @@ def test_pair_full_size_sampled(cuda_lib, name, block, stages):
     R, S = oracle.gemm_entries(A, B, w["dtype"], rows, cols)
     got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
     assert_close(as_f64(got), R, S, w["out"])
+
+
+# ------------------------------------------------------------ two pairs sharing B (multicast)
+
+MCAST_CONFIGS = [
+    ((256, 352, 64), 5),     # a CTA's 88 B rows per N-half in multicast parts of 48 and 40
+    ((256, 512, 64), 4),
+    ((256, 384, 128), 2),    # two K-panels per slot
+    ((256, 256, 64), 4),
+    ((256, 224, 128), 3),    # parts of 56 and 56
+    ((256, 64, 16), 2),      # a 32-row box: parts of 16 and 16
+    ((256, 32, 64), 1),      # the smallest box (16 rows), a one-slot ring
+]
+# tiles_m odd (the cluster's second tile lies past M), one M-block, ragged edges
+MCAST_SHAPES = [(520, 704, 264), (257, 96, 72), (300, 200, 136), (1, 32, 8), (1300, 704, 512)]
+
+
+@pytest.mark.parametrize("block,stages", MCAST_CONFIGS, ids=lambda v: str(v))
+@pytest.mark.parametrize("shape", MCAST_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype,out", [("f16", "f32"), ("bf16", "bf16"), ("f16", "f16")])
+def test_multicast_small_shapes(cuda_lib, block, stages, shape, dtype, out):
+    M, N, K = shape
+    A, B = inputs.operands(300 + M + N + K, M, N, K, dtype, "uniform")
+    C = as_f64(run(cuda_lib, A, B, dtype, out, block, stages, pair=True, multicast_b=True))
+    R, S = oracle.gemm(A, B, dtype)
+    assert_close(C, R, S, out)
+
+
+@pytest.mark.parametrize("block,stages", MCAST_CONFIGS, ids=lambda v: str(v))
+def test_multicast_integer_exact_and_equal_to_pairs(cuda_lib, block, stages):
+    # Same MMAs in the same order as plain CTA pairs: the fp32 results agree
+    # bit for bit, and integer inputs are exact.
+    M, N, K = 1800, 1000, 1032
+    A, B = inputs.operands(43, M, N, K, "bf16", "int", lo=-4, hi=4)
+    two = run(cuda_lib, A, B, "bf16", "f32", block, stages, pair=True)
+    four = run(cuda_lib, A, B, "bf16", "f32", block, stages, pair=True, multicast_b=True)
+    R, _ = oracle.gemm(A, B, "bf16")
+    assert np.array_equal(as_f64(four), R)
+    A, B = inputs.operands(44, M, N, K, "f16", "normal")
+    two = run(cuda_lib, A, B, "f16", "f32", block, stages, pair=True)
+    four = run(cuda_lib, A, B, "f16", "f32", block, stages, pair=True, multicast_b=True)
+    assert torch.equal(two.view(torch.int32), four.view(torch.int32))
+
+
+def test_multicast_plan_geometry(cuda_lib):
+    # Clusters of four CTAs; a work item is two M-adjacent tiles of one N-block.
+    plan = cuda_lib.Plan(4000, 3000, 5000, "f16", "f32", (256, 352, 64), 5, pair=True, multicast_b=True)
+    info = plan.info
+    assert info["multicast_b"] == 1 and info["cta_pair"] == 1
+    assert info["grid"] % 4 == 0 and info["num_units"] == 8 * 9
+    plan.close()
+    rc, h = cuda_lib.tgemm_plan_ex(512, 512, 512, "f16", "f32", 256, 256, 64, 3, cta_pair=0, multicast_b=1)
+    assert rc == cuda_lib.ERR_INVALID_ARG and h is None
+    rc, h = cuda_lib.tgemm_plan_ex(512, 512, 4096, "f16", "f32", 256, 256, 64, 3, cta_pair=1, split_k=4,
+                                   multicast_b=1)
+    assert rc == cuda_lib.ERR_INVALID_ARG and h is None
 
 
 # ------------------------------------------------------------ split-K
@@ -312,11 +369,14 @@ def full_size(cuda_lib, name, block=None, stages=None, pair=False, split_k=1):
     w = inputs.WORKLOADS[name]
     A, B = inputs.workload_operands(name)
     group_m = cluster_k = 0
+    stream_operands = multicast_b = False
     if block is None:
         cfg = cuda_lib.default_config(w["M"], w["N"], w["K"], w["dtype"], w["out"])
         block, stages, pair, split_k = cfg["block"], cfg["num_stages"], cfg["cta_pair"], cfg["split_k"]
         group_m, cluster_k = cfg["group_m"], cfg["cluster_k"]
-    C = run(cuda_lib, A, B, w["dtype"], w["out"], block, stages, pair, split_k, group_m, cluster_k)
+        stream_operands, multicast_b = cfg["stream_operands"], cfg["multicast_b"]
+    C = run(cuda_lib, A, B, w["dtype"], w["out"], block, stages, pair, split_k, group_m, cluster_k, stream_operands,
+            multicast_b)
     return w, A, B, C
 
 

@@ -47,12 +47,13 @@ def draw_cases(tg, n=N_CASES, seed=SEED):
         stages = int(rng.integers(1, 9))
         cluster = int(rng.choice([0, 0, 0, 2, 4]))  # K splits reduced inside the kernel
         stream = int(rng.random() < 0.3)            # L2 evict-first operand loads
+        mcast = int(pair and rng.random() < 0.3)    # two pairs sharing B through multicast
         if tg.tgemm_validate_ex(M, N, K, dtype, out, *block, stages, limit, cta_pair=int(pair),
-                                split_k=split, cluster_k=cluster, stream_operands=stream) != tg.OK:
+                                split_k=split, cluster_k=cluster, stream_operands=stream, multicast_b=mcast) != tg.OK:
             continue
         prefetch = int(rng.integers(1, stages + 1)) if rng.random() < 0.25 else 0
         group = int(rng.choice([0, 0, 1, 2, 3, 16]))
-        cases.append((M, N, K, dtype, out, block, stages, pair, split, prefetch, group, cluster, stream,
+        cases.append((M, N, K, dtype, out, block, stages, pair, split, prefetch, group, cluster, stream, mcast,
                       int(rng.integers(1 << 30))))
     return cases
 
@@ -61,10 +62,10 @@ def test_random_sweep_matches_oracle(cuda_lib):
     tg = cuda_lib
     failures = []
     for i, case in enumerate(draw_cases(tg)):
-        M, N, K, dtype, out, block, stages, pair, split, prefetch, group, cluster, stream, seed = case
+        M, N, K, dtype, out, block, stages, pair, split, prefetch, group, cluster, stream, mcast, seed = case
         A, B = inputs.operands(seed, M, N, K, dtype, "normal")
         plan = tg.Plan(M, N, K, dtype, out, block, stages, pair=pair, split_k=split, prefetch=prefetch,
-                       group_m=group, cluster_k=cluster, stream_operands=stream)
+                       group_m=group, cluster_k=cluster, stream_operands=stream, multicast_b=mcast)
         C = torch.full((M, N), float("nan"), dtype=TORCH[out], device="cuda")
         plan.run(inputs.bits_to_torch(A, dtype).cuda(), inputs.bits_to_torch(B, dtype).cuda(), C)
         torch.cuda.synchronize()

@@ -23,7 +23,8 @@ pytestmark = pytest.mark.gpu
 TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 
 # (block, num_stages, cta_pair, split_k, options): one CTA (64- and 128-row
-# tiles), pairs with one and two K-panels per slot and a wide tile, and the
+# tiles), pairs with one and two K-panels per slot and a wide tile (also with
+# two pairs sharing B through multicast), and the
 # split-K paths whose partials meet in the second kernel, in the GEMM kernel
 # after a grid-wide barrier, or in a cluster through distributed shared memory
 CONFIGS = [
@@ -32,6 +33,7 @@ CONFIGS = [
     ((256, 224, 64), 6, True, 1, {}),
     ((256, 224, 128), 3, True, 1, {"stream_operands": True}),
     ((256, 352, 64), 4, True, 1, {}),
+    ((256, 352, 64), 4, True, 1, {"multicast_b": True}),
     ((256, 256, 128), 3, True, 3, {}),
     ((128, 128, 64), 4, False, 2, {}),
     ((256, 256, 64), 3, True, 3, {"grid_reduce": True}),

@@ -19,7 +19,7 @@ def bits(C):
 
 
 def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=False, group_m=0, split_k=1,
-                        dist="normal", kw=None, cluster_k=0):
+                        dist="normal", kw=None, cluster_k=0, multicast_b=False):
     A, B = inputs.operands(seed, M, N, K, dtype, dist, **(kw or {}))
     dA = inputs.bits_to_torch(A, dtype).cuda()
     dB = inputs.bits_to_torch(B, dtype).cuda()
@@ -27,7 +27,7 @@ def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=F
     res = []
     for s in stage_list:
         plan = tg.Plan(M, N, K, dtype, out, block, s, pair=pair, group_m=group_m, split_k=split_k,
-                       cluster_k=cluster_k)
+                       cluster_k=cluster_k, multicast_b=multicast_b)
         C = torch.full((M, N), float("nan"), dtype=tdt, device="cuda")
         plan.run(dA, dB, C)
         torch.cuda.synchronize()
@@ -85,6 +85,17 @@ def test_bit_identical_across_stages_pair(cuda_lib, block, stage_list):
     res = outputs_over_stages(cuda_lib, 1000, 1040, 2056, "bf16", "f32", block, stage_list, seed=78, pair=True)
     for s, C in zip(stage_list[1:], res[1:]):
         assert torch.equal(bits(C), bits(res[0])), f"num_stages={s} differs"
+
+
+@pytest.mark.parametrize("block,stage_list", [((256, 352, 64), (1, 2, 5)), ((256, 224, 128), (1, 3))])
+def test_bit_identical_across_stages_multicast(cuda_lib, block, stage_list):
+    # Two pairs sharing B through multicast: every depth gives the bits of
+    # plain CTA pairs (odd tiles_m: the cluster's last second tile lies past M).
+    res = outputs_over_stages(cuda_lib, 1300, 1040, 2056, "bf16", "f32", block, stage_list, seed=79, pair=True,
+                              multicast_b=True)
+    ref = outputs_over_stages(cuda_lib, 1300, 1040, 2056, "bf16", "f32", block, stage_list[:1], seed=79, pair=True)
+    for s, C in zip(stage_list, res):
+        assert torch.equal(bits(C), bits(ref[0])), f"num_stages={s} differs"
 
 
 def test_bit_identical_across_prefetch_distances(cuda_lib):

@@ -21,9 +21,10 @@ pytestmark = pytest.mark.gpu
     ((128, 256, 64), 4, False, 8, 4),  # K splits reduced in the kernel by clusters of 4: both cluster levels
     ((256, 256, 64), 3, True, 4, -1),  # K splits reduced in the kernel after a grid-wide barrier
     ((64, 64, 32), 4, False, 1, -2),   # a stream-K tail (1024 x 1024: 256 tiles on 152 CTAs)
+    ((256, 352, 64), 4, True, 1, -3),  # clusters of two pairs sharing B through multicast
 ])
 def test_stall_reports_timeout_and_context_survives(cuda_lib, block, stages, pair, split_k, cluster_k):
-    grid_reduce, stream_k = cluster_k == -1, cluster_k == -2
+    grid_reduce, stream_k, multicast_b = cluster_k == -1, cluster_k == -2, cluster_k == -3
     cluster_k = max(cluster_k, 0)
     M, N, K = (1024, 1024, 512) if stream_k else (512, 512, 512)
     A, B = inputs.operands(31, M, N, K, "f16", "uniform")
@@ -31,7 +32,7 @@ def test_stall_reports_timeout_and_context_survives(cuda_lib, block, stages, pai
     dB = inputs.bits_to_torch(B, "f16").cuda()
     C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
     plan = cuda_lib.Plan(M, N, K, "f16", "f32", block, stages, pair=pair, split_k=split_k, cluster_k=cluster_k,
-                         grid_reduce=grid_reduce, stream_k=stream_k)
+                         grid_reduce=grid_reduce, stream_k=stream_k, multicast_b=multicast_b)
     if stream_k:
         assert plan.info["stream_k_tiles"] > 0
     plan.set_watchdog_ns(50_000_000)
