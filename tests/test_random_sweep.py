@@ -48,6 +48,8 @@ def draw_cases(tg, n=N_CASES, seed=SEED):
         cluster = int(rng.choice([0, 0, 0, 2, 4]))  # K splits reduced inside the kernel
         stream = int(rng.random() < 0.3)            # L2 evict-first operand loads
         mcast = int(pair and rng.random() < 0.3)    # two pairs sharing B through multicast
+        if mcast:
+            split, cluster = 1, 0                   # it takes neither a K split nor the cluster reduction
         if tg.tgemm_validate_ex(M, N, K, dtype, out, *block, stages, limit, cta_pair=int(pair),
                                 split_k=split, cluster_k=cluster, stream_operands=stream, multicast_b=mcast) != tg.OK:
             continue
