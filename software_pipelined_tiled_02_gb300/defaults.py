@@ -79,10 +79,34 @@ def estimate(M: int, N: int, K: int, block, rel: float, num_sms: int = DEFAULT_S
     return waves * bm * bn * max(K, 1) / (2 if pair else 1) / rel
 
 
+# Clusters of four CTAs (two pairs) resident at once on a 152-SM GB300.
+CLUSTERS_OF_FOUR = 36
+
+
+def multicast_pays(M: int, N: int, K: int, block, num_sms: int = DEFAULT_SMS) -> bool:
+    """B shared by two pairs (multicast_b) measured faster where a row of the
+    16-bit operands is not a whole number of 128-byte L2 lines (each box row is
+    then two L2 requests) and the work items, two M-adjacent tiles each, fill
+    rounds of the resident clusters of four no worse than the tiles fill
+    rounds of pairs: 4000x3000x5000, 83.9 against 88.3 us; 2000x3000x5000,
+    46.1 against 47.2 us; 6000x3000x3000 (256x512 tiles), 75.8 either way.
+    Where the rounds grow it was slower (4096^3: 104 against 84 us)."""
+    if (K * 2) % 128 == 0:
+        return False
+    bm, bn, _ = block
+    tiles_m, tiles_n = -(-M // bm), -(-N // bn)
+    clusters = max(1, CLUSTERS_OF_FOUR * num_sms // DEFAULT_SMS)
+    pair_rounds = -(-(tiles_m * tiles_n) // (num_sms // 2))
+    mc_rounds = -(-(-(-tiles_m // 2) * tiles_n) // clusters)
+    return mc_rounds <= pair_rounds
+
+
 def choose(M: int, N: int, K: int, dtype: int, out_dtype: int, num_sms: int = DEFAULT_SMS) -> dict:
-    """{block, num_stages, cta_pair, split_k, group_m, cluster_k, stream_operands} for a problem."""
+    """{block, num_stages, cta_pair, split_k, group_m, cluster_k, stream_operands, grid_reduce, stream_k,
+    multicast_b} for a problem."""
     hit = FROZEN.get((M, N, K, dtype, out_dtype))
     if hit is not None:
         return dict(DEFAULT_OPTS, **hit)
     best = min(CANDIDATES, key=lambda c: (estimate(M, N, K, c[0], c[2], num_sms, c[3]), -c[2]))
-    return dict(DEFAULT_OPTS, block=best[0], num_stages=best[1], cta_pair=best[3])
+    mc = best[3] and multicast_pays(M, N, K, best[0], num_sms)
+    return dict(DEFAULT_OPTS, block=best[0], num_stages=best[1], cta_pair=best[3], multicast_b=mc)

@@ -71,11 +71,11 @@ def pages_prune_count(configs, M, N, K, dtype, budget=PAGES_BUDGET, divisible=Tr
 
 
 def enumerate_space(space: dict):
-    keys = ("block_M", "block_N", "block_K", "num_stages", "cta_pair", "split_k", "stream_operands")
+    keys = ("block_M", "block_N", "block_K", "num_stages", "cta_pair", "split_k", "stream_operands", "multicast_b")
     vals = [space.get(k, (1,) if k == "split_k" else (0,)) for k in keys]
     out = [dict(zip(keys, v)) for v in itertools.product(*vals)]
-    # CTA pairs exist only for block_M = 256 tiles.
-    return [c for c in out if not (c["cta_pair"] and c["block_M"] != 256)]
+    # CTA pairs exist only for block_M = 256 tiles, and B is shared only between pairs.
+    return [c for c in out if not (c["cta_pair"] and c["block_M"] != 256) and not (c["multicast_b"] and not c["cta_pair"])]
 
 
 def prune(configs, M, N, K, dtype, out_dtype, smem_limit, divisible=True):
@@ -90,7 +90,7 @@ def prune(configs, M, N, K, dtype, out_dtype, smem_limit, divisible=True):
         rc = tg.tgemm_validate_ex(M, N, K, dtype, out_dtype, c["block_M"], c["block_N"], c["block_K"],
                                   c["num_stages"], smem_limit, cta_pair=c.get("cta_pair", 0),
                                   split_k=c.get("split_k", 1), cluster_k=c.get("cluster_k", 0),
-                                  stream_operands=c.get("stream_operands", 0))
+                                  stream_operands=c.get("stream_operands", 0), multicast_b=c.get("multicast_b", 0))
         if rc == tg.OK:
             legal.append(c)
         elif rc == tg.ERR_SMEM_BUDGET:
@@ -141,7 +141,7 @@ def write_cache(device_name: str, workload: str, best: dict, rows: list):
     """best_config.json (the winner) and latency.json (every candidate)."""
     os.makedirs(cache_dir(device_name, workload), exist_ok=True)
     keys = ("block_M", "block_N", "block_K", "num_stages", "cta_pair", "split_k", "cluster_k", "stream_operands",
-            "grid_reduce", "prefetch", "median_ms", "min_ms", "tflops", "smem_bytes", "smem_bound", "ok", "worst_error_ratio",
+            "grid_reduce", "multicast_b", "prefetch", "median_ms", "min_ms", "tflops", "smem_bytes", "smem_bound", "ok", "worst_error_ratio",
             "error")
     lat = [{k: r[k] for k in keys if k in r} for r in rows]
     for name, obj in (("best_config.json", best), ("latency.json", lat)):
@@ -188,7 +188,7 @@ class Runner:
                            (c["block_M"], c["block_N"], c["block_K"]), c["num_stages"], pair=bool(c.get("cta_pair")),
                            prefetch=int(c.get("prefetch", 0)), split_k=int(c.get("split_k", 1) or 1),
                            cluster_k=int(c.get("cluster_k", 0)), stream_operands=bool(c.get("stream_operands")),
-                           grid_reduce=bool(c.get("grid_reduce")))
+                           grid_reduce=bool(c.get("grid_reduce")), multicast_b=bool(c.get("multicast_b")))
         except tg.TgemmError as e:
             row.update(ok=False, error=str(e))
             return row
@@ -245,6 +245,7 @@ def main(argv=None):
     ap.add_argument("--stages", default=None, help="only these num_stages, e.g. 2,3,4")
     ap.add_argument("--split-k", default=None, help="K splits to try, e.g. 1,9,19 (default 1)")
     ap.add_argument("--stream", action="store_true", help="also try the L2 evict-first operand hint")
+    ap.add_argument("--multicast", action="store_true", help="also try pair tiles with B shared by two pairs")
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--out", default=None, help="write all rows as JSON here")
     ap.add_argument("--no-cache", action="store_true",
@@ -330,6 +331,8 @@ def main(argv=None):
             space["split_k"] = tuple(int(v) for v in args.split_k.split(","))
         if args.stream:
             space["stream_operands"] = (0, 1)
+        if args.multicast:
+            space["multicast_b"] = (0, 1)
         configs = enumerate_space(space)
         if args.tiles:
             configs = [c for c in configs if (c["block_M"], c["block_N"], c["block_K"]) in tiles]
@@ -347,7 +350,8 @@ def main(argv=None):
         report["best"] = best
         for r in sorted(rows, key=lambda r: r.get("median_ms", 1e9))[:10]:
             print(json.dumps({k: r.get(k) for k in ("block_M", "block_N", "block_K", "num_stages", "cta_pair",
-                                                    "median_ms", "tflops", "smem_bytes", "ok")}), flush=True)
+                                                    "stream_operands", "multicast_b", "median_ms", "tflops",
+                                                    "smem_bytes", "ok")}), flush=True)
         if best and not args.no_cache:
             write_cache(dev, args.workload, best, rows)
             report["cache"] = cache_dir(dev, args.workload)

@@ -82,8 +82,39 @@ def test_frozen_defaults_are_legal_and_chosen():
         assert set(cfg) == {"block", "num_stages"} | set(defaults.DEFAULT_OPTS)
         rc = tg.tgemm_validate_ex(M, N, K, dt, od, *cfg["block"], cfg["num_stages"], 232448,
                                   cta_pair=int(cfg["cta_pair"]), split_k=cfg["split_k"], group_m=cfg["group_m"],
-                                  cluster_k=cfg["cluster_k"], stream_operands=int(cfg["stream_operands"]))
+                                  cluster_k=cfg["cluster_k"], stream_operands=int(cfg["stream_operands"]),
+                                  grid_reduce=int(cfg["grid_reduce"]), stream_k=int(cfg["stream_k"]),
+                                  multicast_b=int(cfg["multicast_b"]))
         assert rc == tg.OK, ((M, N, K), cfg, tg.strerror(rc))
+
+
+def test_multicast_dimension_of_the_space():
+    # B shared by two pairs exists only in pair mode and without a K split.
+    space = dict(sweep.GB300_SPACE, multicast_b=(0, 1), split_k=(1, 2))
+    cfgs = sweep.enumerate_space(space)
+    assert all(c["cta_pair"] for c in cfgs if c["multicast_b"])
+    assert any(c["multicast_b"] for c in cfgs)
+    legal, rej = sweep.prune(cfgs, 4000, 3000, 5000, tg.F16, tg.F32, LIMIT, divisible=False)
+    mc = [c for c in legal if c["multicast_b"]]
+    assert mc and all(c["split_k"] == 1 for c in mc)
+    key = lambda c: (c["block_M"], c["block_N"], c["block_K"], c["num_stages"], c["multicast_b"])  # noqa: E731
+    assert (256, 352, 64, 5, 1) in {key(c) for c in legal}
+    assert any(c["multicast_b"] and c["split_k"] == 2 for c in rej["other"])
+
+
+def test_estimator_shares_b_only_where_rows_straddle_lines_and_rounds_hold():
+    from software_pipelined_tiled_02_gb300 import defaults
+
+    # the frozen ragged shape's reasoning, on its tile: misaligned pitch, 72 items = 2 rounds of 36
+    assert defaults.multicast_pays(4000, 3000, 5000, (256, 352, 64))
+    # the same shape with an aligned pitch (K = 5120): no
+    assert not defaults.multicast_pays(4000, 3000, 5120, (256, 352, 64))
+    # 4096 x 4096 with a misaligned K: 304 tiles are 4 rounds of 76 pairs, 152 items 5 rounds of 36
+    assert not defaults.multicast_pays(4096, 4096, 4100, (256, 224, 128))
+    # a shape outside the table gets it through choose(), and only on pair tiles
+    cfg = defaults.choose(4000, 3000, 5008, tg.F16, tg.F32)
+    assert cfg["cta_pair"] and cfg["multicast_b"] and defaults.multicast_pays(4000, 3000, 5008, cfg["block"])
+    assert not defaults.choose(4096, 4096, 4096 + 8, tg.F16, tg.F16)["multicast_b"]
 
 
 def test_wide_pair_tiles_only_in_pair_mode():
