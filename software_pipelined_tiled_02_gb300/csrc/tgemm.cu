@@ -25,7 +25,8 @@
 //
 // Warp roles (320 threads, one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer (one thread issues)
-//   warp 1      TMEM allocator and tcgen05.mma issuer (one thread issues)
+//   warp 1      TMEM allocator and tcgen05.mma issuer (the converged warp; one
+//               elected lane issues)
 //   warps 2..9  epilogue, two warps per TMEM lane quarter: TMEM -> registers ->
 //               swizzled shared staging -> TMA store
 // The accumulator is double-buffered in TMEM when it fits, so the epilogue of
@@ -34,9 +35,10 @@
 // on num_stages or the schedule, so results are bit-identical across depths.
 //
 // Launch shapes (tgemm_kernel<MODE>): one CTA per tile, or CTA pairs
-// (cta_group::2, M = 256 over two SMs), persistent over work units; or one CTA
-// per (tile, K split) in thread-block clusters that reduce their splits
-// through distributed shared memory.  Split K is otherwise reduced by a
+// (cta_group::2, M = 256 over two SMs), or clusters of two pairs that share B
+// through TMA multicast, persistent over work units; or one CTA per (tile,
+// K split) in thread-block clusters that reduce their splits through
+// distributed shared memory.  Split K is otherwise reduced by a
 // second kernel or, after a grid-wide barrier, by this one.  The persistent
 // schedule can also share the tiles of a partial last wave out by k-blocks
 // (a stream-K tail).  Every such combination adds partial sums in an order
@@ -706,7 +708,7 @@ __device__ __noinline__ void csplit_epilogue(const Params &p, uint32_t sA, int *
     }
 }
 
-// One kernel, three launch shapes.
+// One kernel, four launch shapes.
 //  MODE 0: one CTA per tile, persistent over work units.
 //  MODE 1: clusters of two CTAs; the pair computes one block_M = 256 tile
 //    with one M = 256 MMA per k-step issued by the even CTA, each CTA holding
@@ -720,6 +722,12 @@ __device__ __noinline__ void csplit_epilogue(const Params &p, uint32_t sA, int *
 //    cluster, which sums its partial accumulators through distributed shared
 //    memory (csplit_epilogue); clusters of the same tile then combine through
 //    global memory, the last to arrive adding all in a fixed order.
+//  MODE 3: clusters of four, two CTA pairs as in mode 1 (ranks 0-1 and 2-3)
+//    that take the two M-adjacent tiles of one N-block.  The CTAs of rank r
+//    and r ^ 2 hold the same B rows; each loads one part of them and TMA
+//    multicast writes it into both, completing each receiving pair's even-CTA
+//    full[s].  empty[s] counts both pairs' commits, since a slot holds data of
+//    both; accumulator hand-offs stay within a pair.
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constant__ Params p)
 {
