@@ -2,8 +2,8 @@
 
 The program allocates device memory with the CUDA runtime's C API, plans and runs
 a ragged CTA-pair GEMM on small-integer operands, reads the status and checks every
-output against its own integer products, then exercises the error paths a C
-caller meets.  Integer inputs make the expected values exact.
+output against its own integer products, repeats it with two pairs sharing B
+through multicast, then exercises the error paths a C caller meets.  Integer inputs make the expected values exact.
 """
 
 import os
@@ -74,6 +74,33 @@ int main(void)
             if (hC[(size_t)i * N + j] != (float)s) ++bad;
         }
     if (bad) { printf("%ld wrong outputs\n", bad); return 6; }
+
+    /* the same product with two CTA pairs sharing B through multicast (clusters of four) */
+    tgemm_plan_t mc = 0;
+    opts.multicast_b = 1;
+    rc = tgemm_plan_ex(&mc, M, N, K, TGEMM_F16, TGEMM_F32, 256, 352, 64, 4, &opts);
+    if (rc != TGEMM_OK) { printf("multicast plan: %s\n", tgemm_strerror(rc)); return 11; }
+    tgemm_plan_info info;
+    if (tgemm_get_plan_info(mc, &info) != TGEMM_OK || info.multicast_b != 1 || info.grid % 4 != 0) { puts("info"); return 12; }
+    cudaMemset(dC, 0xFF, nc * 4);
+    if (tgemm_run(mc, dA, dB, dC, 0) != TGEMM_OK) { puts("multicast run"); return 13; }
+    cudaDeviceSynchronize();
+    if (tgemm_status(mc, detail) != TGEMM_OK) { puts("multicast status"); return 14; }
+    cudaMemcpy(hC, dC, nc * 4, cudaMemcpyDeviceToHost);
+    for (int i = 0; i < M; ++i)
+        for (int j = 0; j < N; ++j) {
+            long s = 0;
+            for (int k = 0; k < K; ++k) s += (long)iA[(size_t)i * K + k] * iB[(size_t)j * K + k];
+            if (hC[(size_t)i * N + j] != (float)s) ++bad;
+        }
+    if (bad) { printf("multicast: %ld wrong outputs\n", bad); return 15; }
+    tgemm_destroy(mc);
+    opts.cta_pair = 0;  /* B is shared between pairs only */
+    tgemm_plan_t none = 0;
+    if (tgemm_plan_ex(&none, M, N, K, TGEMM_F16, TGEMM_F32, 256, 352, 64, 4, &opts) != TGEMM_ERR_INVALID_ARG || none) {
+        puts("multicast without pairs");
+        return 16;
+    }
 
     /* error paths: a NULL plan, a misaligned pointer, an over-budget config */
     if (tgemm_run(0, dA, dB, dC, 0) != TGEMM_ERR_INVALID_ARG) { puts("null plan"); return 7; }
