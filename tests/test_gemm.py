@@ -415,6 +415,21 @@ def test_large_coordinates_sampled(cuda_lib, M, N, K, block, stages, split, nran
     assert_close(as_f64(got), R, S, "f32")
 
 
+@pytest.mark.parametrize("M,N,K,block,stages,nrand", [
+    ((1 << 20) + 100, 64, 64, (256, 64, 64), 4, 4096),  # odd M-block count: the last second tile past row 2^20
+    (300, 1 << 18, 128, (256, 512, 64), 4, 4096),       # a quarter-million columns, 512-wide pair tiles
+])
+def test_multicast_large_coordinates_sampled(cuda_lib, M, N, K, block, stages, nrand):
+    A, B = inputs.operands(52, M, N, K, "bf16", "uniform")
+    C = run(cuda_lib, A, B, "bf16", "f32", block, stages, pair=True, multicast_b=True)
+    rows, cols = sample_entries(M, N, nrand, 10)
+    keep = np.arange(rows.size) % 8 == 0  # whole first/last rows and columns of a huge C: a strided subset
+    rows, cols = rows[keep], cols[keep]
+    R, S = oracle.gemm_entries(A, B, "bf16", rows, cols)
+    got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+    assert_close(as_f64(got), R, S, "f32")
+
+
 def test_gemm_convenience_api_uses_tuned_defaults(cuda_lib):
     M, N, K = 512, 512, 32768
     A, B = inputs.operands(52, M, N, K, "f16", "uniform")
