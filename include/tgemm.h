@@ -324,7 +324,7 @@ typedef struct tgemm_plan_info {
     int num_sms;
     int cta_pair;        /* 1: clusters of two CTAs share each tile */
     int split_k;         /* effective K splits (1: none) */
-    int num_units;       /* persistent work units: tiles x K splits */
+    int num_units;       /* persistent work units: tiles x K splits (multicast_b: pairs of tiles) */
     int prefetch;        /* producer lead in k-blocks */
     int cluster_k;       /* > 1: K splits reduced in the kernel by clusters of this many CTAs */
     int stream_operands; /* 1: operand loads carry an L2 evict-first hint */
