@@ -59,6 +59,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <type_traits>
 
 #include "layout.h"
 #include "ptx.cuh"
@@ -811,7 +812,6 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
 
     if (warp == 0) {
         // ---------------- producer: fill the ring, up to num_stages slots ahead.
-        // The whole warp runs the loop (warp-uniform control); lane 0 issues.
         // Pair mode: each CTA loads its own rows of A and B into its own slot;
         // both complete the even CTA's full[s], which the even CTA arms with
         // the bytes of both.
@@ -829,7 +829,109 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         const int D = p.prefetch;
         int sd = S - D;  // slot of iteration issued - D, once issued >= D
         uint32_t phd = 0;
-        for (int i = 0; ok; ++i) {
+        // The whole ring (D = S), the default: lane 0 alone runs a loop whose
+        // tile shape (K-panels per slot, B boxes per panel) and load hint are
+        // compile-time, with the launch constants in registers.  The loop is a
+        // chain of dependent single-thread steps, and each parameter read or
+        // branch in it lengthens the time to refill a slot.
+        auto lean = [&](auto panels_c, auto nh_c, auto stream_c) {
+            constexpr int PANELS = decltype(panels_c)::value;
+            [[maybe_unused]] constexpr int NH = decltype(nh_c)::value;
+            constexpr bool STREAM = decltype(stream_c)::value;
+            const uint32_t a_slot = p.a_slot, b_slot = p.b_slot, tx = p.stage_tx;
+            const uint32_t a_pan = p.a_panel16 << 4, b_pan = p.b_panel16 << 4;
+            [[maybe_unused]] const uint32_t b_half = p.b_half16 << 4;  // a wide tile's second N-half
+            const int bk = p.bk, panel_k = p.panel_k;
+            [[maybe_unused]] const int bnh = p.bn >> 1;
+            const uint32_t part = MC && pidx ? uint32_t(p.b_part0) * p.row_bytes : 0u;
+            const int yp = MC && pidx ? p.b_part0 : 0;
+            [[maybe_unused]] const void *bmap = MC && pidx ? &p.tmB1 : &p.tmB;
+            [[maybe_unused]] const uint16_t mask = uint16_t((1u << crank) | (1u << (crank ^ 2u)));
+            for (int i = 0;; ++i) {
+                Unit w;
+                if (!item(i, w)) break;
+                const int m0 = w.mb * p.bm + int(rank) * p.a_rows;
+                const int n0 = w.nb * p.bn + int(rank) * p.b_box_rows + yp;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!mbar_try_wait(empty(s), ph ^ 1u) && !wait_bar(empty(s), ph ^ 1u, p, abort, 0, issued)) {
+                        ok = false;
+                        return;
+                    }
+                    if (!check(s < S && (kb * bk * 2) % 16 == 0 && kb < p.num_kb &&
+                                   w.mb < (MC ? 2 * p.sched_m : p.tiles_m) && w.nb < p.tiles_n &&
+                                   PANELS * int(a_pan) <= int(a_slot) && PANELS * int(b_pan) <= int(b_slot),
+                               p, abort, 0, issued)) {
+                        ok = false;
+                        return;
+                    }
+                    const uint32_t a_dst = sA + uint32_t(s) * a_slot, b_dst = sB + uint32_t(s) * b_slot + part;
+                    const uint32_t bar = PAIR ? full_leader + 8u * uint32_t(s) : full(s);
+                    if (!PAIR || rank == 0) mbar_arrive_expect_tx(full(s), tx);
+#pragma unroll
+                    for (int pl = 0; pl < PANELS; ++pl) {
+                        const int x = kb * bk + pl * panel_k;
+                        const uint32_t a_at = a_dst + uint32_t(pl) * a_pan, b_at = b_dst + uint32_t(pl) * b_pan;
+                        if constexpr (PAIR) {
+                            if constexpr (STREAM)
+                                tma_load_2d_pair_hint(a_at, &p.tmA, x, m0, bar, policy);
+                            else
+                                tma_load_2d_pair(a_at, &p.tmA, x, m0, bar);
+                            if constexpr (MC) {
+                                // B: this CTA's part of its rows, multicast to it and to the CTA
+                                // of the other pair that holds the same rows (rank ^ 2)
+                                if constexpr (STREAM) {
+                                    tma_load_2d_pair_mc_hint(b_at, bmap, x, n0, bar, mask, policy);
+                                    if constexpr (NH == 2)
+                                        tma_load_2d_pair_mc_hint(b_at + b_half, bmap, x, n0 + bnh, bar, mask, policy);
+                                } else {
+                                    tma_load_2d_pair_mc(b_at, bmap, x, n0, bar, mask);
+                                    if constexpr (NH == 2) tma_load_2d_pair_mc(b_at + b_half, bmap, x, n0 + bnh, bar, mask);
+                                }
+                            } else if constexpr (STREAM) {
+                                tma_load_2d_pair_hint(b_at, &p.tmB, x, n0, bar, policy);
+                                // a wide tile's second N-half: this CTA's rows of it, block_N / 2 further on
+                                if constexpr (NH == 2) tma_load_2d_pair_hint(b_at + b_half, &p.tmB, x, n0 + bnh, bar, policy);
+                            } else {
+                                tma_load_2d_pair(b_at, &p.tmB, x, n0, bar);
+                                if constexpr (NH == 2) tma_load_2d_pair(b_at + b_half, &p.tmB, x, n0 + bnh, bar);
+                            }
+                        } else if constexpr (STREAM) {
+                            tma_load_2d_hint(a_at, &p.tmA, x, m0, bar, policy);
+                            tma_load_2d_hint(b_at, &p.tmB, x, n0, bar, policy);
+                        } else {
+                            tma_load_2d(a_at, &p.tmA, x, m0, bar);
+                            tma_load_2d(b_at, &p.tmB, x, n0, bar);
+                        }
+                    }
+                    ++issued;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        };
+        using One = std::integral_constant<int, 1>;
+        using Two = std::integral_constant<int, 2>;
+        using Plain = std::false_type;
+        using Stream = std::true_type;
+        if (D >= S) {
+            if (lane == 0) {
+                if (p.panels == 2) {
+                    if (p.n_halves == 2)
+                        p.stream_ops ? lean(Two{}, Two{}, Stream{}) : lean(Two{}, Two{}, Plain{});
+                    else
+                        p.stream_ops ? lean(Two{}, One{}, Stream{}) : lean(Two{}, One{}, Plain{});
+                } else if (p.n_halves == 2) {
+                    p.stream_ops ? lean(One{}, Two{}, Stream{}) : lean(One{}, Two{}, Plain{});
+                } else {
+                    p.stream_ops ? lean(One{}, One{}, Stream{}) : lean(One{}, One{}, Plain{});
+                }
+            }
+        }
+        // A prefetch distance D < S: the whole warp runs the loop (warp-uniform
+        // control) and lane 0 issues.
+        for (int i = 0; ok && D < S; ++i) {
             Unit w;
             if (!item(i, w)) break;
             const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn + int(rank) * p.b_box_rows;

@@ -22,19 +22,20 @@ from __future__ import annotations
 # pairs that share B through TMA multicast).  The comments give same-GPU, interleaved timings
 # against the runner-up.
 FROZEN = {
-    # 1643 vs 1607 TFLOP/s for one CTA 256x224x64, group 8
-    (4096, 4096, 4096, 0, 0): dict(block=(256, 224, 128), num_stages=3, cta_pair=True, group_m=2),
-    # 1952-1976 vs 1897-1922 for pair 256x256x128 S3 and 1961-1968 for 256x448x64 (same GPU)
-    (8192, 8192, 8192, 1, 1): dict(block=(256, 512, 64), num_stages=4, cta_pair=True),
+    # 82.1-82.3 us vs 83.7-84.0 for 256x224x128 S3 (same GPU, two GPUs); groups of 4 82.6-82.8
+    (4096, 4096, 4096, 0, 0): dict(block=(256, 224, 64), num_stages=6, cta_pair=True, group_m=2),
+    # 612-615 vs 631-633 us for 256x512x64 S4 and 638-641 for 256x448x64 (same GPU, two GPUs)
+    (8192, 8192, 8192, 1, 1): dict(block=(256, 256, 64), num_stages=6, cta_pair=True),
     # 144 tiles of 256x352 fill two waves of 76 pairs, or with B shared by two pairs (multicast) 72
-    # work items on 36 clusters of four: 84.0 us vs 88.9 for the pairs alone (same GPU), 89.1 for
-    # 256x384x64 S4 with multicast; the 10,000-byte row pitch makes each B row two L2 requests
+    # work items on 36 clusters of four: 82.4 us vs 88.6 for the pairs alone (same GPU), 89.4 for
+    # 256x384x64 S4 with multicast, 97-98 for 256x224x64 S6; the 10,000-byte row pitch makes each
+    # B row two L2 requests
     (4000, 3000, 5000, 0, 2): dict(block=(256, 352, 64), num_stages=5, cta_pair=True, stream_operands=True,
                                    multicast_b=True),
-    # 31.2 vs 33.3 us without the evict-first hint; 35.4 for 128x128x64 S6 split 9; 166 unsplit;
-    # the in-kernel cluster reduction (128x256x64 S4, split 16, clusters of 4) 38.9;
-    # the reduction in the GEMM kernel after a grid-wide barrier 33.3
-    (512, 512, 32768, 0, 2): dict(block=(256, 256, 128), num_stages=3, cta_pair=True, split_k=19,
+    # 64 work units on 64 pairs: 31.1-31.3 us vs 32.1-32.5 for split 19 (76 units) and 32.3-32.6 for
+    # 256x256x128 S3 split 19; splits 12, 14, 18: 32.7-33.1; the reduction after a grid-wide
+    # barrier 32.2; without the evict-first hint 33.4
+    (512, 512, 32768, 0, 2): dict(block=(256, 256, 64), num_stages=6, cta_pair=True, split_k=16,
                                   stream_operands=True),
     (128, 128, 128, 0, 2): dict(block=(128, 128, 32), num_stages=3),
 }
@@ -42,26 +43,35 @@ FROZEN = {
 DEFAULT_OPTS = dict(cta_pair=False, split_k=1, group_m=0, cluster_k=0, stream_operands=False, grid_reduce=False,
                     stream_k=False, multicast_b=False)
 
-# Candidate tiles: (block, depth, relative steady-state throughput per SM,
-# CTA pair), measured on GB300 at whole waves.  A pair computes one 256-row
-# tile on two SMs.  The throughputs follow the operand bytes each SM takes in
-# per cycle at the full tensor rate (69 B for pair 256x224, 64 for 256x256, 48
-# for 256x512): 4096^3 at 256x224 reaches 0.87 of peak, 8192^3 at 256x256
-# 0.97-0.99, 6144^3 at 256x512 1727 against 1706 TFLOP/s for 256x256, and
-# 1024x8192x4096 at 256x448 1397 against 1198 for 256x224x64.  Wide tiles keep
-# one accumulator (no epilogue overlap), which their throughput includes.
+# Candidate tiles: (block, depth, relative steady-state throughput per SM with
+# a row pitch that is a multiple of 128 bytes, the same with one that is not,
+# CTA pair).  Measured on GB300 at whole waves (76 pair tiles or 152 one-CTA
+# tiles, fp16) at K = 16384 and K = 16392, less about 8 us of fixed launch
+# cost; TFLOP/s aligned / misaligned: 256x512 pairs 1966 / 1881, 256x448 pairs
+# 1952 / 1827, 256x256x64 pairs 1927 / 1612, 256x352 1926 / 1743, 256x384
+# 1923 / 1757, one CTA 256x256x64 1953 / 1618, 256x224x64 pairs 1864 / 1520,
+# one CTA 256x224x64 1886 / 1534, 128x256 1689 / 1181, 256x192x64 pairs
+# 1656 / 1404, 128x128 1017 / 844, 128x64 536 / 484.  A misaligned pitch makes
+# each 128-byte box row two L2 requests, which narrow tiles (more operand
+# rows per output) feel most.  A pair computes one 256-row tile on two SMs.
+# The one-CTA 256x224 tile is entered at 0.94 aligned: at K = 1024 and 4096 it
+# ran 6 % behind the 256x224x64 pair.  Wide tiles keep one accumulator (no
+# epilogue overlap), which their throughput includes.  256x256x128 and
+# 256x224x128 pairs (0.95 and 0.89 aligned) are left out: the same tiles at
+# block_K = 64 and six stages are faster.
 CANDIDATES = (
-    ((256, 256, 128), 3, 0.99, True),
-    ((256, 512, 64), 4, 1.00, True),   # two N = 256 MMAs per k-step sharing A
-    ((256, 448, 64), 4, 1.00, True),
-    ((256, 384, 64), 4, 0.98, True),   # measured on 4000x3000x5000
-    ((256, 352, 64), 5, 0.97, True),   # two N = 176 MMAs per k-step
-    ((256, 224, 128), 3, 0.88, True),
-    ((256, 256, 64), 3, 0.95, False),
-    ((256, 224, 64), 3, 0.85, False),
-    ((128, 256, 64), 4, 0.80, False),
-    ((128, 128, 64), 4, 0.55, False),
-    ((128, 64, 64), 4, 0.32, False),
+    ((256, 512, 64), 4, 1.00, 0.96, True),   # two N = 256 MMAs per k-step sharing A
+    ((256, 448, 64), 4, 0.99, 0.93, True),
+    ((256, 256, 64), 6, 0.98, 0.82, True),
+    ((256, 384, 64), 4, 0.98, 0.89, True),
+    ((256, 352, 64), 5, 0.98, 0.89, True),   # two N = 176 MMAs per k-step
+    ((256, 256, 64), 3, 0.99, 0.82, False),
+    ((256, 224, 64), 6, 0.95, 0.77, True),
+    ((256, 224, 64), 3, 0.94, 0.78, False),
+    ((128, 256, 64), 4, 0.86, 0.60, False),
+    ((256, 192, 64), 6, 0.84, 0.71, True),
+    ((128, 128, 64), 4, 0.52, 0.43, False),
+    ((128, 64, 64), 4, 0.27, 0.25, False),
 )
 
 DEFAULT_SMS = 152
@@ -88,9 +98,10 @@ def multicast_pays(M: int, N: int, K: int, block, num_sms: int = DEFAULT_SMS) ->
     16-bit operands is not a whole number of 128-byte L2 lines (each box row is
     then two L2 requests) and the work items, two M-adjacent tiles each, fill
     rounds of the resident clusters of four no worse than the tiles fill
-    rounds of pairs: 4000x3000x5000, 83.9 against 88.3 us; 2000x3000x5000,
+    rounds of pairs: 4000x3000x5000, 82.4 against 88.6 us; 2000x3000x5000,
     46.1 against 47.2 us; 6000x3000x3000 (256x512 tiles), 75.8 either way.
-    Where the rounds grow it was slower (4096^3: 104 against 84 us)."""
+    Where the rounds grow it was slower (4096^3, 256x224x128 tiles: 101.4
+    against 83.5 us)."""
     if (K * 2) % 128 == 0:
         return False
     bm, bn, _ = block
@@ -107,6 +118,7 @@ def choose(M: int, N: int, K: int, dtype: int, out_dtype: int, num_sms: int = DE
     hit = FROZEN.get((M, N, K, dtype, out_dtype))
     if hit is not None:
         return dict(DEFAULT_OPTS, **hit)
-    best = min(CANDIDATES, key=lambda c: (estimate(M, N, K, c[0], c[2], num_sms, c[3]), -c[2]))
-    mc = best[3] and multicast_pays(M, N, K, best[0], num_sms)
-    return dict(DEFAULT_OPTS, block=best[0], num_stages=best[1], cta_pair=best[3], multicast_b=mc)
+    col = 2 if (K * 2) % 128 == 0 else 3  # 16-bit operands: a row pitch of 2K bytes
+    best = min(CANDIDATES, key=lambda c: (estimate(M, N, K, c[0], c[col], num_sms, c[4]), -c[col]))
+    mc = best[4] and multicast_pays(M, N, K, best[0], num_sms)
+    return dict(DEFAULT_OPTS, block=best[0], num_stages=best[1], cta_pair=best[4], multicast_b=mc)

@@ -113,8 +113,15 @@ def test_estimator_shares_b_only_where_rows_straddle_lines_and_rounds_hold():
     assert not defaults.multicast_pays(4096, 4096, 4100, (256, 224, 128))
     # a shape outside the table gets it through choose(), and only on pair tiles
     cfg = defaults.choose(4000, 3000, 5008, tg.F16, tg.F32)
+    assert cfg["block"] == (256, 352, 64)
     assert cfg["cta_pair"] and cfg["multicast_b"] and defaults.multicast_pays(4000, 3000, 5008, cfg["block"])
-    assert not defaults.choose(4096, 4096, 4096 + 8, tg.F16, tg.F16)["multicast_b"]
+    # where the chosen pair tile's rounds would grow, no multicast: 2 x 37 tiles of 256x512 are one round of
+    # 76 pairs but 37 items on 36 clusters; 16 x 14 tiles of 256x448 are 3 rounds, 112 items 4
+    for M, N in ((512, 18944), (4096, 6144)):
+        cfg = defaults.choose(M, N, 4104, tg.F16, tg.F16)
+        assert cfg["cta_pair"] and not cfg["multicast_b"] and not defaults.multicast_pays(M, N, 4104, cfg["block"])
+    # with an aligned pitch, never
+    assert not defaults.choose(4096, 4096, 4096 + 64, tg.F16, tg.F16)["multicast_b"]
 
 
 def test_wide_pair_tiles_only_in_pair_mode():
@@ -154,20 +161,56 @@ def test_write_and_read_cache(tmp_path, monkeypatch):
 
 
 def test_estimator_picks_the_measured_best_tiles():
-    # Shapes outside the tuned table: the wave-count estimator chose, on a
-    # GB300, the same tile as a timed search over its candidates.
+    # Shapes outside the tuned table: the candidate the wave-count estimator
+    # picks ran within 3 % of the fastest tile of a timed search on a GB300
+    # (mean CUDA-event microseconds, fp16 in and out, 256 MiB L2 flush before
+    # each launch; the one-CTA 256x224 and the block_K = 128 pair tiles were
+    # timed as well but are no longer candidates).
     from software_pipelined_tiled_02_gb300 import defaults
 
-    measured_best = {
-        (3072, 3072, 3072): (256, 512, 64),
-        (6144, 6144, 6144): (256, 512, 64),
-        (1024, 8192, 4096): (256, 448, 64),
-        (8192, 1024, 4096): (256, 512, 64),
-        (4096, 4096, 1024): (256, 224, 128),
-        (2048, 2048, 2048): (256, 256, 128),
+    P, O = True, False
+    measured = {
+        (3072, 3072, 3072): {
+            ((256, 256, 128), 3, P): 41.8, ((256, 512, 64), 4, P): 41.2, ((256, 448, 64), 4, P): 64.1,
+            ((256, 384, 64), 4, P): 57.7, ((256, 352, 64), 5, P): 53.7, ((256, 224, 128), 3, P): 51.8,
+            ((256, 256, 64), 6, P): 40.8, ((256, 224, 64), 6, P): 50.0, ((256, 192, 64), 6, P): 49.0,
+            ((256, 128, 64), 8, P): 58.3, ((256, 256, 64), 3, O): 41.3, ((256, 224, 64), 3, O): 65.3,
+            ((128, 256, 64), 4, O): 44.1, ((128, 128, 64), 4, O): 62.8},
+        (6144, 6144, 6144): {
+            ((256, 256, 128), 3, P): 273.4, ((256, 512, 64), 4, P): 275.3, ((256, 448, 64), 4, P): 298.3,
+            ((256, 384, 64), 4, P): 308.1, ((256, 352, 64), 5, P): 284.6, ((256, 224, 128), 3, P): 273.1,
+            ((256, 256, 64), 6, P): 270.2, ((256, 224, 64), 6, P): 273.1, ((256, 192, 64), 6, P): 310.7,
+            ((256, 128, 64), 8, P): 427.2, ((256, 256, 64), 3, O): 282.8, ((256, 224, 64), 3, O): 321.0,
+            ((128, 256, 64), 4, O): 323.0, ((128, 128, 64), 4, O): 506.7},
+        (1024, 8192, 4096): {
+            ((256, 256, 128), 3, P): 53.7, ((256, 512, 64), 4, P): 50.3, ((256, 448, 64), 4, P): 47.9,
+            ((256, 384, 64), 4, P): 74.3, ((256, 352, 64), 5, P): 66.9, ((256, 224, 128), 3, P): 52.5,
+            ((256, 256, 64), 6, P): 51.3, ((256, 224, 64), 6, P): 48.8, ((256, 192, 64), 6, P): 62.8,
+            ((256, 128, 64), 8, P): 74.1, ((256, 256, 64), 3, O): 53.4, ((256, 224, 64), 3, O): 50.5,
+            ((128, 256, 64), 4, O): 61.2, ((128, 128, 64), 4, O): 88.9},
+        (8192, 1024, 4096): {
+            ((256, 256, 128), 3, P): 53.7, ((256, 512, 64), 4, P): 49.6, ((256, 448, 64), 4, P): 80.2,
+            ((256, 384, 64), 4, P): 72.6, ((256, 352, 64), 5, P): 66.2, ((256, 224, 128), 3, P): 67.2,
+            ((256, 256, 64), 6, P): 51.4, ((256, 224, 64), 6, P): 63.7, ((256, 192, 64), 6, P): 62.0,
+            ((256, 128, 64), 8, P): 74.1, ((256, 256, 64), 3, O): 53.4, ((256, 224, 64), 3, O): 83.7,
+            ((128, 256, 64), 4, O): 58.6, ((128, 128, 64), 4, O): 78.4},
+        (4096, 4096, 1024): {
+            ((256, 256, 128), 3, P): 33.1, ((256, 512, 64), 4, P): 38.1, ((256, 448, 64), 4, P): 45.3,
+            ((256, 384, 64), 4, P): 43.4, ((256, 352, 64), 5, P): 40.3, ((256, 224, 128), 3, P): 31.2,
+            ((256, 256, 64), 6, P): 31.9, ((256, 224, 64), 6, P): 31.2, ((256, 192, 64), 6, P): 35.0,
+            ((256, 128, 64), 8, P): 40.2, ((256, 256, 64), 3, O): 35.8, ((256, 224, 64), 3, O): 33.2,
+            ((128, 256, 64), 4, O): 33.2, ((128, 128, 64), 4, O): 41.2},
+        (2048, 2048, 2048): {
+            ((256, 256, 128), 3, P): 21.7, ((256, 512, 64), 4, P): 31.1, ((256, 448, 64), 4, P): 28.9,
+            ((256, 384, 64), 4, P): 26.3, ((256, 352, 64), 5, P): 24.9, ((256, 224, 128), 3, P): 28.0,
+            ((256, 256, 64), 6, P): 21.1, ((256, 224, 64), 6, P): 27.1, ((256, 192, 64), 6, P): 27.9,
+            ((256, 128, 64), 8, P): 27.0, ((256, 256, 64), 3, O): 31.1, ((256, 224, 64), 3, O): 29.1,
+            ((128, 256, 64), 4, O): 21.6, ((128, 128, 64), 4, O): 27.1},
     }
-    for (M, N, K), block in measured_best.items():
+    for (M, N, K), times in measured.items():
         cfg = defaults.choose(M, N, K, tg.F16, tg.F16)
-        assert cfg["block"] == block and cfg["cta_pair"], ((M, N, K), cfg)
+        key = (cfg["block"], cfg["num_stages"], cfg["cta_pair"])
+        assert key in times, ((M, N, K), key)
+        assert times[key] <= 1.03 * min(times.values()), ((M, N, K), key, times[key], min(times.values()))
         assert tg.tgemm_validate_ex(M, N, K, tg.F16, tg.F16, *cfg["block"], cfg["num_stages"], 232448,
-                                    cta_pair=1) == tg.OK
+                                    cta_pair=int(cfg["cta_pair"])) == tg.OK
