@@ -125,8 +125,9 @@ int tgemm_validate(int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, in
  * by the caller (free it with tgemm_destroy); on failure *out is NULL.  The
  * pages' analogue is matmul(M, N, K, block_M, block_N, block_K, num_stages,
  * ...) of chapter 11 section 3.5; its `threads` argument has no counterpart
- * because the kernel's warp roles fix the block at 320 threads (a TMA producer
- * warp, an MMA warp and eight epilogue warps).
+ * because the kernel's warp roles fix the block at 352 threads (two TMA
+ * producer warps, one for A and one for B, an MMA warp and eight epilogue
+ * warps).
  */
 int tgemm_plan(tgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
                int block_M, int block_N, int block_K, int num_stages);

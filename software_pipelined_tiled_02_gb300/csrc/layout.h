@@ -23,7 +23,9 @@ enum : int {
 
 enum : int { kF16 = 0, kBF16 = 1, kF32 = 2 };
 
-constexpr int kThreads = 320;         // 10 warps: TMA producer, MMA issuer, 8 epilogue warps
+constexpr int kThreads = 352;         // 11 warps: TMA producer (A), MMA issuer, 8 epilogue warps,
+                                      // TMA producer (B)
+constexpr int kProducerBWarp = 10;    // the warp that loads B
 constexpr int kEpiWarps = 8;          // two per TMEM lane quarter, splitting the column chunks
 constexpr int kEpiCols = 32;          // accumulator columns per epilogue chunk
 constexpr int kTmemColsMax = 512;     // tensor-memory columns per SM

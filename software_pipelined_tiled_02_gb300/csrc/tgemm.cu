@@ -810,8 +810,12 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------- producer: fill the ring, up to num_stages slots ahead.
+    if (warp == 0 || warp == kProducerBWarp) {
+        // ---------------- producers: fill the ring, up to num_stages slots ahead.
+        // Warp 0 arms each slot and loads A, warp 10 loads B: a pair-mode
+        // (cta_group::2) TMA load takes about 120 cycles to issue, so one
+        // thread issuing both operands refilled a block_K = 64 slot more
+        // slowly than the MMAs drained it.
         // Pair mode: each CTA loads its own rows of A and B into its own slot;
         // both complete the even CTA's full[s], which the even CTA arms with
         // the bytes of both.
@@ -829,15 +833,19 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         const int D = p.prefetch;
         int sd = S - D;  // slot of iteration issued - D, once issued >= D
         uint32_t phd = 0;
-        // The whole ring (D = S), the default: lane 0 alone runs a loop whose
-        // tile shape (K-panels per slot, B boxes per panel) and load hint are
-        // compile-time, with the launch constants in registers.  The loop is a
-        // chain of dependent single-thread steps, and each parameter read or
-        // branch in it lengthens the time to refill a slot.
-        auto lean = [&](auto panels_c, auto nh_c, auto stream_c) {
+        // The whole ring (D = S), the default: lane 0 of each producer warp
+        // alone runs a loop whose operand, tile shape (K-panels per slot, B
+        // boxes per panel) and load hint are compile-time, with the launch
+        // constants in registers.  The loop is a chain of dependent
+        // single-thread steps, and each parameter read or branch in it
+        // lengthens the time to refill a slot.  Both warps wait for the same
+        // empty[s]; B bytes that land before warp 0 arms the phase only take
+        // its transaction count below zero until the arming arrives.
+        auto lean = [&](auto panels_c, auto nh_c, auto stream_c, auto part_c) {
             constexpr int PANELS = decltype(panels_c)::value;
             [[maybe_unused]] constexpr int NH = decltype(nh_c)::value;
             constexpr bool STREAM = decltype(stream_c)::value;
+            constexpr bool LOAD_A = decltype(part_c)::value == 0;  // else B
             const uint32_t a_slot = p.a_slot, b_slot = p.b_slot, tx = p.stage_tx;
             const uint32_t a_pan = p.a_panel16 << 4, b_pan = p.b_panel16 << 4;
             [[maybe_unused]] const uint32_t b_half = p.b_half16 << 4;  // a wide tile's second N-half
@@ -866,16 +874,23 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                     }
                     const uint32_t a_dst = sA + uint32_t(s) * a_slot, b_dst = sB + uint32_t(s) * b_slot + part;
                     const uint32_t bar = PAIR ? full_leader + 8u * uint32_t(s) : full(s);
-                    if (!PAIR || rank == 0) mbar_arrive_expect_tx(full(s), tx);
+                    if (LOAD_A && (!PAIR || rank == 0)) mbar_arrive_expect_tx(full(s), tx);
 #pragma unroll
                     for (int pl = 0; pl < PANELS; ++pl) {
                         const int x = kb * bk + pl * panel_k;
                         const uint32_t a_at = a_dst + uint32_t(pl) * a_pan, b_at = b_dst + uint32_t(pl) * b_pan;
-                        if constexpr (PAIR) {
-                            if constexpr (STREAM)
-                                tma_load_2d_pair_hint(a_at, &p.tmA, x, m0, bar, policy);
-                            else
-                                tma_load_2d_pair(a_at, &p.tmA, x, m0, bar);
+                        if constexpr (LOAD_A) {
+                            if constexpr (PAIR) {
+                                if constexpr (STREAM)
+                                    tma_load_2d_pair_hint(a_at, &p.tmA, x, m0, bar, policy);
+                                else
+                                    tma_load_2d_pair(a_at, &p.tmA, x, m0, bar);
+                            } else if constexpr (STREAM) {
+                                tma_load_2d_hint(a_at, &p.tmA, x, m0, bar, policy);
+                            } else {
+                                tma_load_2d(a_at, &p.tmA, x, m0, bar);
+                            }
+                        } else if constexpr (PAIR) {
                             if constexpr (MC) {
                                 // B: this CTA's part of its rows, multicast to it and to the CTA
                                 // of the other pair that holds the same rows (rank ^ 2)
@@ -896,10 +911,8 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                                 if constexpr (NH == 2) tma_load_2d_pair(b_at + b_half, &p.tmB, x, n0 + bnh, bar);
                             }
                         } else if constexpr (STREAM) {
-                            tma_load_2d_hint(a_at, &p.tmA, x, m0, bar, policy);
                             tma_load_2d_hint(b_at, &p.tmB, x, n0, bar, policy);
                         } else {
-                            tma_load_2d(a_at, &p.tmA, x, m0, bar);
                             tma_load_2d(b_at, &p.tmB, x, n0, bar);
                         }
                     }
@@ -915,23 +928,28 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         using Two = std::integral_constant<int, 2>;
         using Plain = std::false_type;
         using Stream = std::true_type;
-        if (D >= S) {
-            if (lane == 0) {
-                if (p.panels == 2) {
-                    if (p.n_halves == 2)
-                        p.stream_ops ? lean(Two{}, Two{}, Stream{}) : lean(Two{}, Two{}, Plain{});
-                    else
-                        p.stream_ops ? lean(Two{}, One{}, Stream{}) : lean(Two{}, One{}, Plain{});
-                } else if (p.n_halves == 2) {
-                    p.stream_ops ? lean(One{}, Two{}, Stream{}) : lean(One{}, Two{}, Plain{});
-                } else {
-                    p.stream_ops ? lean(One{}, One{}, Stream{}) : lean(One{}, One{}, Plain{});
-                }
+        using PartA = std::integral_constant<int, 0>;
+        using PartB = std::integral_constant<int, 1>;
+        if (D >= S && lane == 0) {
+            if (warp == 0) {
+                if (p.panels == 2)
+                    p.stream_ops ? lean(Two{}, One{}, Stream{}, PartA{}) : lean(Two{}, One{}, Plain{}, PartA{});
+                else
+                    p.stream_ops ? lean(One{}, One{}, Stream{}, PartA{}) : lean(One{}, One{}, Plain{}, PartA{});
+            } else if (p.panels == 2) {
+                if (p.n_halves == 2)
+                    p.stream_ops ? lean(Two{}, Two{}, Stream{}, PartB{}) : lean(Two{}, Two{}, Plain{}, PartB{});
+                else
+                    p.stream_ops ? lean(Two{}, One{}, Stream{}, PartB{}) : lean(Two{}, One{}, Plain{}, PartB{});
+            } else if (p.n_halves == 2) {
+                p.stream_ops ? lean(One{}, Two{}, Stream{}, PartB{}) : lean(One{}, Two{}, Plain{}, PartB{});
+            } else {
+                p.stream_ops ? lean(One{}, One{}, Stream{}, PartB{}) : lean(One{}, One{}, Plain{}, PartB{});
             }
         }
-        // A prefetch distance D < S: the whole warp runs the loop (warp-uniform
-        // control) and lane 0 issues.
-        for (int i = 0; ok && D < S; ++i) {
+        // A prefetch distance D < S: warp 0 loads both operands; the whole
+        // warp runs the loop (warp-uniform control) and lane 0 issues.
+        for (int i = 0; ok && D < S && warp == 0; ++i) {
             Unit w;
             if (!item(i, w)) break;
             const int m0 = w.mb * p.bm + int(rank) * p.a_rows, n0 = w.nb * p.bn + int(rank) * p.b_box_rows;
@@ -1021,10 +1039,12 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
         }
         if (!ok && lane == 0) {
             // Let the loads still in flight land before the CTA may exit:
-            // only the last min(S, issued) slots can be outstanding.  In mode 3
-            // a CTA's B copies also land in the other pair, whose barriers it
-            // cannot wait on: every CTA takes the fixed wait below.
-            if (!MC && (!PAIR || rank == 0)) {
+            // only the last min(S, issued) slots can be outstanding.  With
+            // two producer warps a slot may hold one warp's loads only (the
+            // other gave up first), and in mode 3 a CTA's B copies also land in
+            // the other pair, whose barriers it cannot wait on: there the
+            // fixed wait below.
+            if (D < S && !MC && (!PAIR || rank == 0)) {
                 const int first = issued > S ? issued - S : 0;
                 for (int j = first; j < issued; ++j)
                     wait_bar(full(j % S), uint32_t((j / S) & 1), p, abort, 0, j, false);
