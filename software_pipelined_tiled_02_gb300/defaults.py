@@ -32,10 +32,10 @@ FROZEN = {
     # B row two L2 requests
     (4000, 3000, 5000, 0, 2): dict(block=(256, 352, 64), num_stages=5, cta_pair=True, stream_operands=True,
                                    multicast_b=True),
-    # 64 work units on 64 pairs: 31.1-31.3 us vs 32.1-32.5 for split 19 (76 units) and 32.3-32.6 for
-    # 256x256x128 S3 split 19; splits 12, 14, 18: 32.7-33.1; the reduction after a grid-wide
-    # barrier 32.2; without the evict-first hint 33.4
-    (512, 512, 32768, 0, 2): dict(block=(256, 256, 64), num_stages=6, cta_pair=True, split_k=16,
+    # 8 tiles x 9 splits = 72 work units on 76 pairs: 30.0 us vs 30.2-30.6 for 256x128x64 S8 split 9,
+    # 31.6-31.9 for 256x256x64 S6 split 16 and for one CTA 128x256x64 split 19, 33.2 for 256x256x64
+    # split 19; the reduction after a grid-wide barrier 31.7-31.9; without the evict-first hint 34.6-34.9
+    (512, 512, 32768, 0, 2): dict(block=(256, 128, 128), num_stages=4, cta_pair=True, split_k=9,
                                   stream_operands=True),
     (128, 128, 128, 0, 2): dict(block=(128, 128, 32), num_stages=3),
 }
