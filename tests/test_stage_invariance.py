@@ -19,7 +19,7 @@ def bits(C):
 
 
 def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=False, group_m=0, split_k=1,
-                        dist="normal", kw=None, cluster_k=0, multicast_b=False):
+                        dist="normal", kw=None, cluster_k=0, multicast_b=False, stream_operands=False):
     A, B = inputs.operands(seed, M, N, K, dtype, dist, **(kw or {}))
     dA = inputs.bits_to_torch(A, dtype).cuda()
     dB = inputs.bits_to_torch(B, dtype).cuda()
@@ -27,7 +27,7 @@ def outputs_over_stages(tg, M, N, K, dtype, out, block, stage_list, seed, pair=F
     res = []
     for s in stage_list:
         plan = tg.Plan(M, N, K, dtype, out, block, s, pair=pair, group_m=group_m, split_k=split_k,
-                       cluster_k=cluster_k, multicast_b=multicast_b)
+                       cluster_k=cluster_k, multicast_b=multicast_b, stream_operands=stream_operands)
         C = torch.full((M, N), float("nan"), dtype=tdt, device="cuda")
         plan.run(dA, dB, C)
         torch.cuda.synchronize()
@@ -56,17 +56,19 @@ def test_bit_identical_across_stages(cuda_lib, block, stage_list, dtype, out):
                                   "gemm_4000x3000x5000_f16_uniform", "gemm_512x512x32768_f16_uniform"])
 def test_bit_identical_across_stages_benchmark_config(cuda_lib, name):
     # The launch configuration the benchmark times (tile, CTA pair, raster
-    # group, K splits), at every depth that fits its tile.
+    # group, K splits, multicast, load hint), at every depth that fits its tile.
     w = inputs.WORKLOADS[name]
     cfg = cuda_lib.default_config(w["M"], w["N"], w["K"], w["dtype"], w["out"])
-    stage_list = [s for s in (1, 2, 3, 4, 6) if s <= cfg["num_stages"] and
+    stage_list = [s for s in (1, 2, 3, 4, 5, 6) if s <= cfg["num_stages"] and
                   cuda_lib.tgemm_validate_ex(w["M"], w["N"], w["K"], w["dtype"], w["out"], *cfg["block"], s, 232448,
                                              cta_pair=int(cfg["cta_pair"]), split_k=cfg["split_k"],
-                                             cluster_k=cfg["cluster_k"]) == cuda_lib.OK]
-    assert len(stage_list) >= 2
+                                             cluster_k=cfg["cluster_k"], multicast_b=int(cfg["multicast_b"]),
+                                             stream_operands=int(cfg["stream_operands"])) == cuda_lib.OK]
+    assert len(stage_list) >= 2 and stage_list[-1] == cfg["num_stages"]
     res = outputs_over_stages(cuda_lib, w["M"], w["N"], w["K"], w["dtype"], w["out"], cfg["block"], stage_list,
                               w["seed"], pair=cfg["cta_pair"], group_m=cfg["group_m"], split_k=cfg["split_k"],
-                              dist=w["dist"], kw=w.get("kw"), cluster_k=cfg["cluster_k"])
+                              dist=w["dist"], kw=w.get("kw"), cluster_k=cfg["cluster_k"],
+                              multicast_b=cfg["multicast_b"], stream_operands=cfg["stream_operands"])
     for s, C in zip(stage_list[1:], res[1:]):
         assert torch.equal(bits(C), bits(res[0])), f"num_stages={s} differs"
 
@@ -79,6 +81,7 @@ def test_bit_identical_across_stages_4096(cuda_lib):
 
 @pytest.mark.parametrize("block,stage_list", [((256, 256, 64), (1, 2, 4, 6)), ((256, 128, 32), (1, 3, 8)),
                                               ((256, 224, 128), (1, 2, 3)), ((256, 512, 64), (1, 2, 4)),
+                                              ((256, 224, 64), (1, 3, 6)), ((256, 128, 128), (1, 2, 4)),
                                               ((256, 352, 64), (1, 2, 4)),
                                               ((256, 448, 128), (1, 2))])
 def test_bit_identical_across_stages_pair(cuda_lib, block, stage_list):
