@@ -40,8 +40,8 @@ struct Layout {
     int in_bytes, out_bytes;
     uint32_t a_stage_bytes;  // bm * bk * in_bytes
     uint32_t b_stage_bytes;  // bn * bk * in_bytes
-    uint32_t c_buf_bytes;    // one staging buffer: 32 rows x kEpiCols x out_bytes
-    int epi_bufs;            // staging buffers per epilogue warp: 2 for 16-bit C, 1 for fp32 C
+    uint32_t c_buf_bytes;    // one staging buffer: one store box, 32 rows of 64 bytes (32 16-bit or 16 fp32 columns)
+    int epi_bufs;            // staging buffers per epilogue warp: 2
     uint32_t off_a, off_b, off_c, off_bar;
     uint32_t bar_bytes;
     uint32_t total;          // bytes requested, including alignment slack
@@ -104,8 +104,8 @@ inline Layout make_layout(int bm, int bn, int bk, int stages, int dtype, int out
     L.b_stage_bytes = uint32_t(L.b_rows) * bk * L.in_bytes;
     // The pages' bound for the operand tiles one CTA (one block) holds.
     L.bound = int64_t(stages) * (int64_t(L.a_rows) * bk + int64_t(bk) * L.b_rows) * L.in_bytes;
-    L.c_buf_bytes = 32u * kEpiCols * L.out_bytes;
-    L.epi_bufs = L.out_bytes == 4 ? 1 : 2;
+    L.c_buf_bytes = 32u * 64u;
+    L.epi_bufs = 2;
     L.off_a = 0;
     L.off_b = L.off_a + uint32_t(stages) * round_up(L.a_stage_bytes, kSmemAlign);
     L.off_c = L.off_b + uint32_t(stages) * round_up(L.b_stage_bytes, kSmemAlign);

@@ -1210,49 +1210,52 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
                                 v[4 * e + 3] = __float_as_uint(acc[e].w);
                             }
                         }
-                        const uint32_t buf = my_bufs + (nbuf == 2 ? (chunk & 1u) : 0u) * p.c_buf_bytes;
-                        if (chunk >= uint32_t(nbuf) && lane == 0) {  // buffer's previous store has read it
-                            if (nbuf == 2)
-                                bulk_wait_read<1>();
-                            else
-                                bulk_wait_read<0>();
-                        }
-                        __syncwarp();
-                        if (p.out_mode == 0) {
-                            // fp32: 128-byte rows, 128-byte swizzle (16-byte chunk j of row r at j ^ (r % 8))
-                            const uint32_t row = buf + uint32_t(lane) * 128u;
+                        // Staging: each TMA store box is 32 rows of 64 bytes (32 16-bit or 16 fp32
+                        // columns; 64-byte swizzle, 16-byte piece j of row r at j ^ ((r / 2) % 4)) in one
+                        // of this warp's two buffers, so a box is staged while the previous box's store
+                        // still reads the other buffer.  A 32-column chunk is one box of 16-bit output
+                        // and two of fp32.
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                st_shared_v4(row + (uint32_t(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1],
-                                             v[4 * j + 2], v[4 * j + 3]);
-                        } else {
-                            // 16-bit: 64-byte rows, 64-byte swizzle (chunk j of row r at j ^ ((r / 2) % 4))
+                        for (int bx = 0; bx < 2; ++bx) {
+                            const int bcol = col0 + bx * (kEpiCols / 2);
+                            if (bx == 1 && (p.out_mode != 0 || bcol >= p.N)) break;  // warp-uniform
+                            const uint32_t buf = my_bufs + (chunk & 1u) * p.c_buf_bytes;
+                            if (chunk >= 2u && lane == 0) bulk_wait_read<1>();  // its previous store has read it
+                            __syncwarp();
                             const uint32_t row = buf + uint32_t(lane) * 64u;
+                            if (p.out_mode == 0) {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                uint32_t hw[4];
+                                for (int j = 0; j < 4; ++j)
+                                    st_shared_v4(row + (uint32_t(j ^ ((lane >> 1) & 3)) << 4), v[16 * bx + 4 * j],
+                                                 v[16 * bx + 4 * j + 1], v[16 * bx + 4 * j + 2], v[16 * bx + 4 * j + 3]);
+                            } else {
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float x0 = __uint_as_float(v[8 * j + 2 * e]);
-                                    const float x1 = __uint_as_float(v[8 * j + 2 * e + 1]);
-                                    if (p.out_mode == 1) {
-                                        __half2 h2 = __floats2half2_rn(x0, x1);
-                                        hw[e] = *reinterpret_cast<uint32_t *>(&h2);
-                                    } else {
-                                        __nv_bfloat162 b2 = __floats2bfloat162_rn(x0, x1);
-                                        hw[e] = *reinterpret_cast<uint32_t *>(&b2);
+                                for (int j = 0; j < 4; ++j) {
+                                    uint32_t hw[4];
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float x0 = __uint_as_float(v[8 * j + 2 * e]);
+                                        const float x1 = __uint_as_float(v[8 * j + 2 * e + 1]);
+                                        if (p.out_mode == 1) {
+                                            __half2 h2 = __floats2half2_rn(x0, x1);
+                                            hw[e] = *reinterpret_cast<uint32_t *>(&h2);
+                                        } else {
+                                            __nv_bfloat162 b2 = __floats2bfloat162_rn(x0, x1);
+                                            hw[e] = *reinterpret_cast<uint32_t *>(&b2);
+                                        }
                                     }
+                                    st_shared_v4(row + (uint32_t(j ^ ((lane >> 1) & 3)) << 4), hw[0], hw[1], hw[2],
+                                                 hw[3]);
                                 }
-                                st_shared_v4(row + (uint32_t(j ^ ((lane >> 1) & 3)) << 4), hw[0], hw[1], hw[2], hw[3]);
                             }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&p.tmC, bcol, w.row_off + row0, buf);
+                                bulk_commit();
+                            }
+                            ++chunk;
                         }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&p.tmC, col0, w.row_off + row0, buf);
-                            bulk_commit();
-                        }
-                        ++chunk;
                     }
                 }
             };
@@ -1568,14 +1571,14 @@ static int encode_maps(Params &q, const Layout &L, int dtype, int out_dtype, con
             rc = encode_2d(&q.tmB1, dtype, B, K, N, pitch, box_k, b_box - part0, swz, operand_promotion(pitch));
     }
     if (rc != kOk) return rc;
-    // one store box per epilogue chunk: kEpiCols columns of one warp's accumulator rows
+    // one store box per staging buffer: 64 bytes (32 16-bit or 16 fp32 columns) of one warp's
+    // accumulator rows, 64-byte swizzle
     const uint32_t box_rows = uint32_t(L.quarter_rows);
     if (q.splits > 1 && q.csk == 0)
         return encode_2d(&q.tmC, kF32, work, N, uint64_t(q.splits) * uint64_t(q.split_rows), N * 4u,
-                         uint32_t(kEpiCols), box_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
-    return encode_2d(&q.tmC, out_dtype, C, N, M, N * uint64_t(L.out_bytes), uint32_t(kEpiCols), box_rows,
-                     L.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                     CU_TENSOR_MAP_L2_PROMOTION_NONE);
+                         uint32_t(kEpiCols / 2), box_rows, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    return encode_2d(&q.tmC, out_dtype, C, N, M, N * uint64_t(L.out_bytes), uint32_t(64 / L.out_bytes), box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // Ranges of the plan options (NULL: all defaults).
