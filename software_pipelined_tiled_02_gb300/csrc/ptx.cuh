@@ -398,6 +398,14 @@ __device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr)
     return v;
 }
 
+// Programmatic dependent launch.  launch_dependents lets a kernel launched
+// after this one with programmatic stream serialisation be scheduled once
+// every CTA of this grid has issued it (or exited); wait blocks until the
+// grid this kernel depends on has completed and its memory is visible (at
+// once when launched without that attribute).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)

@@ -809,6 +809,9 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
     if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // A split-K reduction launched after this kernel may be scheduled from now
+    // on; it waits for this grid's completion before it reads the partials.
+    griddep_launch_dependents();
 
     if (warp == 0 || warp == kProducerBWarp) {
         // ---------------- producers: fill the ring, up to num_stages slots ahead.
@@ -1318,6 +1321,7 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ W, void *__restrict__ C,
                                                             int64_t mn, int64_t stride, int splits, int out_mode)
 {
+    griddep_wait();  // launched as a programmatic dependent of the GEMM: its partials are complete
     const int64_t n4 = mn / 4;
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
         float4 acc = reinterpret_cast<const float4 *>(W)[i];
@@ -1969,9 +1973,23 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
         if (blocks > cap) blocks = cap;
         const int out_mode = p->out_dtype == kF32 ? 0 : p->out_dtype == kF16 ? 1 : 2;
         const int64_t stride = int64_t(p->params.split_rows) * p->N;
-        splitk_reduce_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p->d_work, C, mn, stride,
-                                                                                         p->splits, out_mode);
-        if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+        // A programmatic dependent of the GEMM: it is scheduled while the GEMM's
+        // CTAs finish and waits in the kernel for the GEMM grid to complete.
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3(unsigned(blocks), 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, static_cast<const float *>(p->d_work), C, mn, stride,
+                               p->splits, out_mode) != cudaSuccess) {
+            cudaGetLastError();
+            return kErrCuda;
+        }
     }
     return kOk;
 }
