@@ -809,8 +809,12 @@ __global__ void __launch_bounds__(kThreads, 1) tgemm_kernel(const __grid_constan
     if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // A split-K reduction launched after this kernel may be scheduled from now
-    // on; it waits for this grid's completion before it reads the partials.
+    // Launched as a programmatic dependent of the kernel before it, this one may
+    // have started while that kernel finished: nothing above touched global
+    // memory, and nothing below may before that kernel's writes are visible.
+    griddep_wait();
+    // A split-K reduction (or another GEMM) launched after this kernel may be
+    // scheduled from now on; it waits for this grid's completion in turn.
     griddep_launch_dependents();
 
     if (warp == 0 || warp == kProducerBWarp) {
@@ -1932,8 +1936,13 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
         // Clusters for CTA pairs and the cluster reduction; a cooperative
         // launch (every CTA resident at once) for the grid-wide reduction.
         cudaLaunchConfig_t cfg{};
-        cudaLaunchAttribute attr[2];
+        cudaLaunchAttribute attr[3];
         unsigned na = 0;
+        if (!p->grid_reduce) {  // see the one-CTA launch below
+            attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[na].val.programmaticStreamSerializationAllowed = 1;
+            ++na;
+        }
         if (p->pair || p->csk) {
             attr[na].id = cudaLaunchAttributeClusterDimension;
             attr[na].val.clusterDim.x = p->csk ? unsigned(p->csk) : p->mc ? 4u : 2u;
@@ -1962,8 +1971,24 @@ int tgemm_run(tgemm_plan_t p, const void *A, const void *B, void *C, tgemm_strea
             return kErrCuda;
         }
     } else {
-        tgemm_kernel<0><<<p->grid, kThreads, p->smem_launch, reinterpret_cast<cudaStream_t>(stream)>>>(p->params);
-        if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+        // A programmatic dependent of the kernel before it in the stream: its
+        // launch and set-up overlap that kernel's last CTAs, and it waits in
+        // griddepcontrol.wait before it reads A and B or writes C.  (The
+        // cooperative launch of the grid-wide reduction keeps the plain order.)
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3(unsigned(p->grid), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = size_t(p->smem_launch);
+        cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, tgemm_kernel<0>, p->params) != cudaSuccess) {
+            cudaGetLastError();
+            return kErrCuda;
+        }
     }
     if (p->splits > 1 && !p->csk && !p->grid_reduce) {
         const int64_t mn = p->M * p->N;
