@@ -6,7 +6,7 @@ turn tuning off.  ``FROZEN`` holds the sweep's winners (``sweep.py`` on a
 GB300, compute capability 10.3, 152 SMs) for the measured workloads; other
 shapes take the candidate tile with the smallest estimated makespan: whole
 waves of persistent tiles (ceil(tiles / SMs)) times the tile's work over its
-measured relative throughput.  The estimate only ranks candidates, as the
+measured relative throughput, plus the epilogues that no MMAs overlap.  The estimate only ranks candidates, as the
 pages say of cost models; the sweep decides.
 """
 
@@ -51,7 +51,8 @@ DEFAULT_OPTS = dict(cta_pair=False, split_k=1, group_m=0, cluster_k=0, stream_op
 # 1952 / 1827, 256x256x64 pairs 1927 / 1612, 256x352 1926 / 1743, 256x384
 # 1923 / 1757, one CTA 256x256x64 1953 / 1618, 256x224x64 pairs 1864 / 1520,
 # one CTA 256x224x64 1886 / 1534, 128x256 1689 / 1181, 256x192x64 pairs
-# 1656 / 1404, 128x128 1017 / 844, 128x64 536 / 484.  A misaligned pitch makes
+# 1656 / 1404, 128x128 1017 / 844, 128x64 536 / 484 (re-measured with two
+# producer warps: each within 2 %, 256x192 pairs 3 % up).  A misaligned pitch makes
 # each 128-byte box row two L2 requests, which narrow tiles (more operand
 # rows per output) feel most.  A pair computes one 256-row tile on two SMs.
 # The one-CTA 256x224 tile is entered at 0.94 aligned: at K = 1024 and 4096 it
@@ -77,16 +78,34 @@ CANDIDATES = (
 DEFAULT_SMS = 152
 
 
+# An epilogue that no MMAs overlap costs about as much as this many K-steps of the
+# tile's own MMAs (its output and its MMA rate both scale with block_N).  Fitted to
+# the timed searches below the tuned table: 6144^3 needs more than 143 to prefer
+# 256x256 pairs (2 accumulators) to 256x512 (1), 8192x1024x4096 less than 168 to
+# keep 256x512.
+EPILOGUE_K = 155
+
+
+def accumulators(block, pair: bool = False) -> int:
+    """Accumulators a tile keeps in TMEM (512 columns): two when twice its
+    columns fit, so that a tile's epilogue overlaps the next tile's MMAs."""
+    bm, bn, _ = block
+    cols = (1 if pair or bm < 256 else 2) * bn
+    return 2 if 2 * cols <= 512 else 1
+
+
 def estimate(M: int, N: int, K: int, block, rel: float, num_sms: int = DEFAULT_SMS, pair: bool = False) -> float:
     """Relative makespan of a persistent launch of this tile (arbitrary units).
 
     A pair works on one tile with two SMs: half as many tiles run at once,
-    each in half the time."""
+    each in half the time.  Every tile's epilogue is exposed with one
+    accumulator, only the last with two."""
     bm, bn, _ = block
     tiles = -(-M // bm) * -(-N // bn)
     slots = num_sms // 2 if pair else num_sms
     waves = -(-tiles // slots)
-    return waves * bm * bn * max(K, 1) / (2 if pair else 1) / rel
+    exposed = waves if accumulators(block, pair) == 1 else 1
+    return bm * bn / (2 if pair else 1) * (waves * max(K, 1) / rel + EPILOGUE_K * exposed)
 
 
 # Clusters of four CTAs (two pairs) resident at once on a 152-SM GB300.

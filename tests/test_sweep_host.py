@@ -163,49 +163,49 @@ def test_write_and_read_cache(tmp_path, monkeypatch):
 def test_estimator_picks_the_measured_best_tiles():
     # Shapes outside the tuned table: the candidate the wave-count estimator
     # picks ran within 3 % of the fastest tile of a timed search on a GB300
-    # (mean CUDA-event microseconds, fp16 in and out, 256 MiB L2 flush before
-    # each launch; the one-CTA 256x224 and the block_K = 128 pair tiles were
+    # with two producer warps (mean CUDA-event microseconds, fp16 in and out,
+    # 256 MiB L2 flush before each launch; the block_K = 128 pair tiles were
     # timed as well but are no longer candidates).
     from software_pipelined_tiled_02_gb300 import defaults
 
     P, O = True, False
     measured = {
         (3072, 3072, 3072): {
-            ((256, 256, 128), 3, P): 41.8, ((256, 512, 64), 4, P): 41.2, ((256, 448, 64), 4, P): 64.1,
-            ((256, 384, 64), 4, P): 57.7, ((256, 352, 64), 5, P): 53.7, ((256, 224, 128), 3, P): 51.8,
-            ((256, 256, 64), 6, P): 40.8, ((256, 224, 64), 6, P): 50.0, ((256, 192, 64), 6, P): 49.0,
-            ((256, 128, 64), 8, P): 58.3, ((256, 256, 64), 3, O): 41.3, ((256, 224, 64), 3, O): 65.3,
-            ((128, 256, 64), 4, O): 44.1, ((128, 128, 64), 4, O): 62.8},
+            ((256, 256, 128), 3, P): 42.2, ((256, 512, 64), 4, P): 41.7, ((256, 448, 64), 4, P): 65.4,
+            ((256, 384, 64), 4, P): 58.7, ((256, 352, 64), 5, P): 54.8, ((256, 224, 128), 3, P): 52.1,
+            ((256, 256, 64), 6, P): 41.4, ((256, 224, 64), 6, P): 50.3, ((256, 192, 64), 6, P): 47.0,
+            ((256, 128, 64), 8, P): 52.0, ((256, 256, 64), 3, O): 41.4, ((256, 224, 64), 3, O): 65.0,
+            ((128, 256, 64), 4, O): 45.1, ((128, 128, 64), 4, O): 61.6},
         (6144, 6144, 6144): {
-            ((256, 256, 128), 3, P): 273.4, ((256, 512, 64), 4, P): 275.3, ((256, 448, 64), 4, P): 298.3,
-            ((256, 384, 64), 4, P): 308.1, ((256, 352, 64), 5, P): 284.6, ((256, 224, 128), 3, P): 273.1,
-            ((256, 256, 64), 6, P): 270.2, ((256, 224, 64), 6, P): 273.1, ((256, 192, 64), 6, P): 310.7,
-            ((256, 128, 64), 8, P): 427.2, ((256, 256, 64), 3, O): 282.8, ((256, 224, 64), 3, O): 321.0,
-            ((128, 256, 64), 4, O): 323.0, ((128, 128, 64), 4, O): 506.7},
+            ((256, 256, 128), 3, P): 273.8, ((256, 512, 64), 4, P): 281.4, ((256, 448, 64), 4, P): 306.6,
+            ((256, 384, 64), 4, P): 315.1, ((256, 352, 64), 5, P): 291.4, ((256, 224, 128), 3, P): 271.5,
+            ((256, 256, 64), 6, P): 267.5, ((256, 224, 64), 6, P): 266.4, ((256, 192, 64), 6, P): 285.2,
+            ((256, 128, 64), 8, P): 362.5, ((256, 256, 64), 3, O): 280.6, ((256, 224, 64), 3, O): 312.5,
+            ((128, 256, 64), 4, O): 317.1, ((128, 128, 64), 4, O): 485.9},
         (1024, 8192, 4096): {
-            ((256, 256, 128), 3, P): 53.7, ((256, 512, 64), 4, P): 50.3, ((256, 448, 64), 4, P): 47.9,
-            ((256, 384, 64), 4, P): 74.3, ((256, 352, 64), 5, P): 66.9, ((256, 224, 128), 3, P): 52.5,
-            ((256, 256, 64), 6, P): 51.3, ((256, 224, 64), 6, P): 48.8, ((256, 192, 64), 6, P): 62.8,
-            ((256, 128, 64), 8, P): 74.1, ((256, 256, 64), 3, O): 53.4, ((256, 224, 64), 3, O): 50.5,
-            ((128, 256, 64), 4, O): 61.2, ((128, 128, 64), 4, O): 88.9},
+            ((256, 256, 128), 3, P): 53.7, ((256, 512, 64), 4, P): 51.1, ((256, 448, 64), 4, P): 48.3,
+            ((256, 384, 64), 4, P): 74.9, ((256, 352, 64), 5, P): 68.2, ((256, 224, 128), 3, P): 52.0,
+            ((256, 256, 64), 6, P): 51.7, ((256, 224, 64), 6, P): 48.9, ((256, 192, 64), 6, P): 60.3,
+            ((256, 128, 64), 8, P): 65.1, ((256, 256, 64), 3, O): 52.3, ((256, 224, 64), 3, O): 50.0,
+            ((128, 256, 64), 4, O): 60.0, ((128, 128, 64), 4, O): 86.2},
         (8192, 1024, 4096): {
-            ((256, 256, 128), 3, P): 53.7, ((256, 512, 64), 4, P): 49.6, ((256, 448, 64), 4, P): 80.2,
-            ((256, 384, 64), 4, P): 72.6, ((256, 352, 64), 5, P): 66.2, ((256, 224, 128), 3, P): 67.2,
-            ((256, 256, 64), 6, P): 51.4, ((256, 224, 64), 6, P): 63.7, ((256, 192, 64), 6, P): 62.0,
-            ((256, 128, 64), 8, P): 74.1, ((256, 256, 64), 3, O): 53.4, ((256, 224, 64), 3, O): 83.7,
-            ((128, 256, 64), 4, O): 58.6, ((128, 128, 64), 4, O): 78.4},
+            ((256, 256, 128), 3, P): 54.1, ((256, 512, 64), 4, P): 50.2, ((256, 448, 64), 4, P): 80.4,
+            ((256, 384, 64), 4, P): 73.1, ((256, 352, 64), 5, P): 67.3, ((256, 224, 128), 3, P): 67.6,
+            ((256, 256, 64), 6, P): 51.9, ((256, 224, 64), 6, P): 63.8, ((256, 192, 64), 6, P): 60.2,
+            ((256, 128, 64), 8, P): 66.3, ((256, 256, 64), 3, O): 52.8, ((256, 224, 64), 3, O): 84.4,
+            ((128, 256, 64), 4, O): 58.5, ((128, 128, 64), 4, O): 76.6},
         (4096, 4096, 1024): {
-            ((256, 256, 128), 3, P): 33.1, ((256, 512, 64), 4, P): 38.1, ((256, 448, 64), 4, P): 45.3,
-            ((256, 384, 64), 4, P): 43.4, ((256, 352, 64), 5, P): 40.3, ((256, 224, 128), 3, P): 31.2,
-            ((256, 256, 64), 6, P): 31.9, ((256, 224, 64), 6, P): 31.2, ((256, 192, 64), 6, P): 35.0,
-            ((256, 128, 64), 8, P): 40.2, ((256, 256, 64), 3, O): 35.8, ((256, 224, 64), 3, O): 33.2,
-            ((128, 256, 64), 4, O): 33.2, ((128, 128, 64), 4, O): 41.2},
+            ((256, 256, 128), 3, P): 33.2, ((256, 512, 64), 4, P): 38.6, ((256, 448, 64), 4, P): 45.7,
+            ((256, 384, 64), 4, P): 43.5, ((256, 352, 64), 5, P): 41.2, ((256, 224, 128), 3, P): 31.6,
+            ((256, 256, 64), 6, P): 32.1, ((256, 224, 64), 6, P): 30.9, ((256, 192, 64), 6, P): 33.3,
+            ((256, 128, 64), 8, P): 37.5, ((256, 256, 64), 3, O): 36.2, ((256, 224, 64), 3, O): 33.4,
+            ((128, 256, 64), 4, O): 33.5, ((128, 128, 64), 4, O): 39.3},
         (2048, 2048, 2048): {
-            ((256, 256, 128), 3, P): 21.7, ((256, 512, 64), 4, P): 31.1, ((256, 448, 64), 4, P): 28.9,
-            ((256, 384, 64), 4, P): 26.3, ((256, 352, 64), 5, P): 24.9, ((256, 224, 128), 3, P): 28.0,
-            ((256, 256, 64), 6, P): 21.1, ((256, 224, 64), 6, P): 27.1, ((256, 192, 64), 6, P): 27.9,
-            ((256, 128, 64), 8, P): 27.0, ((256, 256, 64), 3, O): 31.1, ((256, 224, 64), 3, O): 29.1,
-            ((128, 256, 64), 4, O): 21.6, ((128, 128, 64), 4, O): 27.1},
+            ((256, 256, 128), 3, P): 22.1, ((256, 512, 64), 4, P): 31.1, ((256, 448, 64), 4, P): 29.0,
+            ((256, 384, 64), 4, P): 26.8, ((256, 352, 64), 5, P): 25.0, ((256, 224, 128), 3, P): 28.7,
+            ((256, 256, 64), 6, P): 21.3, ((256, 224, 64), 6, P): 27.1, ((256, 192, 64), 6, P): 26.9,
+            ((256, 128, 64), 8, P): 24.9, ((256, 256, 64), 3, O): 29.6, ((256, 224, 64), 3, O): 28.9,
+            ((128, 256, 64), 4, O): 21.5, ((128, 128, 64), 4, O): 26.9},
     }
     for (M, N, K), times in measured.items():
         cfg = defaults.choose(M, N, K, tg.F16, tg.F16)
@@ -214,3 +214,21 @@ def test_estimator_picks_the_measured_best_tiles():
         assert times[key] <= 1.03 * min(times.values()), ((M, N, K), key, times[key], min(times.values()))
         assert tg.tgemm_validate_ex(M, N, K, tg.F16, tg.F16, *cfg["block"], cfg["num_stages"], 232448,
                                     cta_pair=int(cfg["cta_pair"])) == tg.OK
+
+
+def test_accumulator_count_and_exposed_epilogues():
+    from software_pipelined_tiled_02_gb300 import defaults
+
+    # TMEM holds 512 columns; a tile keeps two accumulators when twice its columns fit
+    assert defaults.accumulators((256, 256, 64), pair=True) == 2
+    assert defaults.accumulators((256, 512, 64), pair=True) == 1      # two N-halves of 256
+    assert defaults.accumulators((256, 256, 64), pair=False) == 1     # two M-halves of 256 columns
+    assert defaults.accumulators((256, 128, 64), pair=False) == 2
+    assert defaults.accumulators((128, 256, 64), pair=False) == 2
+    # one accumulator exposes every tile's epilogue, two only the last one
+    e = defaults.EPILOGUE_K
+    one = defaults.estimate(4096, 4096, 1000, (256, 512, 64), 1.0, pair=True)      # 128 tiles: 2 waves
+    two = defaults.estimate(4096, 4096, 1000, (256, 256, 64), 1.0, pair=True)      # 256 tiles: 4 waves
+    assert one == 256 * 512 / 2 * (2 * 1000 + 2 * e)
+    assert two == 256 * 256 / 2 * (4 * 1000 + 1 * e)
+
