@@ -29,13 +29,14 @@ FROZEN = {
     # 144 tiles of 256x352 fill two waves of 76 pairs, or with B shared by two pairs (multicast) 72
     # work items on 36 clusters of four: 82.4 us vs 88.6 for the pairs alone (same GPU), 89.4 for
     # 256x384x64 S4 with multicast, 97-98 for 256x224x64 S6; the 10,000-byte row pitch makes each
-    # B row two L2 requests
+    # B row two L2 requests.  Raster groups of 4: 81.1-81.2 us vs 82.1 for 8, 82.2-82.3 for 2
     (4000, 3000, 5000, 0, 2): dict(block=(256, 352, 64), num_stages=5, cta_pair=True, stream_operands=True,
-                                   multicast_b=True),
-    # 8 tiles x 9 splits = 72 work units on 76 pairs: 30.0 us vs 30.2-30.6 for 256x128x64 S8 split 9,
-    # 31.6-31.9 for 256x256x64 S6 split 16 and for one CTA 128x256x64 split 19, 33.2 for 256x256x64
-    # split 19; the reduction after a grid-wide barrier 31.7-31.9; without the evict-first hint 34.6-34.9
-    (512, 512, 32768, 0, 2): dict(block=(256, 128, 128), num_stages=4, cta_pair=True, split_k=9,
+                                   multicast_b=True, group_m=4),
+    # 8 tiles x 8 splits = 64 work units on 64 pairs: 29.1-29.3 us vs 29.5-29.6 for 9 splits (72 units),
+    # 29.4-29.5 for 256x128x64 S8 split 9, 31.6-31.9 for 256x256x64 S6 split 16 and for one CTA
+    # 128x256x64 split 19, 33.2 for 256x256x64 split 19; 9 splits with the reduction after a
+    # grid-wide barrier 31.7-31.9; without the evict-first hint 34.6-34.9
+    (512, 512, 32768, 0, 2): dict(block=(256, 128, 128), num_stages=4, cta_pair=True, split_k=8,
                                   stream_operands=True),
     (128, 128, 128, 0, 2): dict(block=(128, 128, 32), num_stages=3),
 }
