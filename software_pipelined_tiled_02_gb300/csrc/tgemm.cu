@@ -18,17 +18,22 @@
 //    landed (transaction count), empty[s] completes when the MMAs that read
 //    the slot have finished (tcgen05.commit);
 //  * the prologue / steady state / epilogue of section 4.3 are implicit: the
-//    producer warp runs up to num_stages k-blocks ahead of the MMA warp and
-//    blocks only on empty[s];
+//    producer warps run up to num_stages k-blocks ahead of the MMA warp and
+//    block only on empty[s];
 //  * num_stages = 1 is the unpipelined control of section 1.1 (copy and math
 //    serialise on the single slot).
 //
-// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
-//   warp 0      TMA producer (one thread issues)
+// Warp roles (352 threads, one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer of A, which also arms each slot's full barrier
+//               (lane 0 runs the loop alone)
+//   warp 10     TMA producer of B (lane 0 runs the loop alone)
 //   warp 1      TMEM allocator and tcgen05.mma issuer (the converged warp; one
 //               elected lane issues)
 //   warps 2..9  epilogue, two warps per TMEM lane quarter: TMEM -> registers ->
 //               swizzled shared staging -> TMA store
+// Each launch is a programmatic dependent of the kernel before it in the
+// stream: the set-up overlaps that kernel's end, and every thread waits for
+// its writes (griddepcontrol.wait) before any global memory access.
 // The accumulator is double-buffered in TMEM when it fits, so the epilogue of
 // tile i overlaps the main loop of tile i+1.  The summation order inside a
 // tile depends only on the tile shape (k-block by k-block, 16 at a time), never
