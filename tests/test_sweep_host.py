@@ -49,6 +49,28 @@ def test_pick_best_tie_break():
     assert sweep.pick_best([dict(ok=False)]) is None
 
 
+def test_pick_best_ranks_by_mean():
+    # CUDA event timestamps advance in steps of about 2 us: two candidates can share a
+    # median while their means differ; the mean decides, and the footprint rule still
+    # applies within 1 % of the fastest mean.
+    rows = [dict(ok=True, mean_ms=0.0830, median_ms=0.0820, smem_bytes=200000, num_stages=6),
+            dict(ok=True, mean_ms=0.0812, median_ms=0.0820, smem_bytes=210000, num_stages=6),
+            dict(ok=True, mean_ms=0.0815, median_ms=0.0840, smem_bytes=150000, num_stages=3)]
+    assert sweep.pick_best(rows)["smem_bytes"] == 150000   # within 1 % of 0.0812, smaller footprint
+    rows[2]["mean_ms"] = 0.0830
+    assert sweep.pick_best(rows)["smem_bytes"] == 210000   # the lowest mean alone
+
+
+def test_raster_group_dimension():
+    space = dict(block_M=(256,), block_N=(224,), block_K=(64,), num_stages=(6,), cta_pair=(1,), group_m=(2, 4, 8))
+    cfgs = sweep.enumerate_space(space)
+    assert sorted(c["group_m"] for c in cfgs) == [2, 4, 8]
+    legal, rej = sweep.prune(cfgs, 4096, 4096, 4096, tg.F16, tg.F16, LIMIT, divisible=False)
+    assert len(legal) == 3
+    # without the key every config takes the library's group (0 = 8)
+    assert all(c["group_m"] == 0 for c in sweep.enumerate_space(dict(space, group_m=(0,))))
+
+
 def test_cache_switch(tmp_path, monkeypatch):
     monkeypatch.setenv("TGEMM_CACHE_DIR", str(tmp_path))
     p = sweep.cache_path("NVIDIA GB300", "wl")
